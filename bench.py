@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the lookahead sparse decode hot path on one GB300.
+
+A step is one decode step of one layer of the Qwen3-8B-shaped workload
+(batch 8, 32 q / 8 KV heads, d_h 128, 32,768-token context = 2,048 blocks of
+16, K = 128, 3 draft queries, fetch ratio 0.05 -> cap 7): compressed-key
+update of the newest block, draft-query block scoring, top-K selection with
+capped eviction, staging of the admitted blocks from pinned host memory, and
+sparse decode attention - every step in liboasis.so's kernels, on three CUDA
+streams ordered by events.
+
+Metric: HBM GB/s = (summaries read + selected K/V read + fp32 outputs written)
+per step / step time; also microseconds per step and the fraction of the
+measured HBM copy bandwidth reached by the dominant kernel.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own copy of the workload (weak scaling; the
+segments are independent, no data-path collective) and rank 0 prints one JSON
+line with the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "lookahead select + sparse decode-attn: HBM GB/s, µs/step, % of GB300 roofline"
+WORKLOAD_ID = 2
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--rotate", type=int, default=4, help="independent buffer sets cycled to defeat L2")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (CPU baseline)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _config(w, extra=None):
+    c = {"workload": f"{w.name}: 1 layer, batch {w.B}, {w.Hq} q / {w.Hkv} KV heads, d_h {w.D}, context {w.L} "
+                     f"({w.Nb} blocks of 16), K={w.K}, W={w.W}, {w.Nd} drafts, fetch_ratio {w.fetch_ratio} "
+                     f"(cap {w.cap}), bf16 KV, fp32 scores/out",
+         "bytes_per_step": w.headline_bytes_per_layer(),
+         "segments": w.S}
+    if extra:
+        c.update(extra)
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sms.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# --------------------------------------------------------------------------- CPU (oracle) side
+
+def _oracle_setup(w, n_seg):
+    """Inputs of n_seg segments for the oracle (untimed): tiles, summaries, prior table."""
+    import numpy as np
+    import torch
+
+    from oracle.score import score_blocks
+    from oracle.select import top_k
+    from oracle.summary import block_summary
+    from synth import workload as wl
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    qd, qt = u16(wl.drafts(w, 0)), u16(wl.q_true(w, 0))
+    segs = sorted({int(round(i * (w.S - 1) / max(1, n_seg - 1))) for i in range(n_seg)})
+    prep = []
+    for seg in segs:
+        b, h = divmod(seg, w.Hkv)
+        tiles = u16(wl.kv_tiles(w, 0, [seg])[0])
+        kmin, kmax, _ = block_summary(tiles[:, 0], w.L)
+        tk = top_k(score_blocks(kmin[:w.nc], kmax[:w.nc], qt[b, h * w.G:(h + 1) * w.G]), w.K)
+        prep.append((seg, tiles, kmin, kmax, wl.prior_from_topk(w, 0, seg, tk).tolist()))
+    return qd, qt, prep
+
+
+def _oracle_sample(w, seconds, setup, start=0):
+    """Run the oracle's decode step on the prepared segments, cycling, until
+    `seconds` of CPU time are spent; returns (headline bytes, seconds, segment-steps)."""
+    import numpy as np
+
+    from oracle import pipeline as opipe
+    from oracle.score import segment_queries
+
+    qd, qt, prep = setup
+    scale = float(np.float32(1.0 / math.sqrt(w.D)))
+    per_seg = w.headline_bytes_per_layer() // w.S
+    done, elapsed, i = 0, 0.0, start
+    while elapsed < seconds:
+        seg, tiles, kmin, kmax, table = prep[i % len(prep)]
+        b, h = divmod(seg, w.Hkv)
+        t0 = time.perf_counter()
+        opipe.run_segment(tiles, w.L, segment_queries(qd, b, h, w.G), qt[b, h * w.G:(h + 1) * w.G], table,
+                          w.K, w.W, w.cap, scale, kmin=kmin.copy(), kmax=kmax.copy(), update_blocks=[w.Nb - 1])
+        elapsed += time.perf_counter() - t0
+        done += 1
+        i += 1
+    return done * per_seg, elapsed, done
+
+
+def _cpu_baseline(w, seconds):
+    setup = _oracle_setup(w, 4)
+    nbytes, secs, nseg = _oracle_sample(w, seconds, setup)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nseg} segment-steps cycling over {len(setup[2])} of the {w.S} segments of one decode "
+                      f"step (newest-block summary update, scoring, capped selection, staging, attention); "
+                      f"single-threaded numpy oracle, {secs:.1f} s; value = headline bytes of the sample / time",
+            "us_per_step_equiv": secs / nseg * w.S * 1e6}
+
+
+def run_reference(args):
+    from synth import workload as wl
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = wl.WORKLOADS[WORKLOAD_ID]
+    setup = _oracle_setup(w, 4)
+    budget = min(5.0, max(0.5, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_sample(w, budget / 4, setup)
+    total_b, total_s, segs = 0, 0.0, 0
+    for i in range(args.steps):
+        nb, s, n = _oracle_sample(w, budget, setup, start=i)
+        total_b, total_s, segs = total_b + nb, total_s + s, segs + n
+    value = total_b / total_s / 1e9
+    ms = total_s / segs * w.S * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": _config(w, {"sample": f"{segs} segments over {args.steps} steps"}),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{segs} segment-steps cycling over {len(setup[2])} segments, "
+                                       f"single-threaded numpy oracle, {total_s:.1f} s timed"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU side
+
+def _gpu_prior(w, lay, tiles, sl, q):
+    """Prior resident tables (about 90 % of the true-query top-K), computed with the kernels."""
+    import torch
+
+    import sparse_kv_cache_quest_gb300 as okv
+    from synth import workload as wl
+    S = w.S
+    scores = torch.zeros((S, w.Nb), dtype=torch.float32, device="cuda")
+    okv.oasis_score_blocks(lay.kmin, lay.kmax, w.Nb, q.view(w.B, 1, w.Hq, w.D), w.B, w.Hkv, w.G, 1, w.D, sl, w.W,
+                           scores, lay.status)
+    empty = torch.full((S, w.slots), -1, dtype=torch.int32, device="cuda")
+    if w.W:
+        empty[:, w.K:] = torch.tensor(wl.window_blocks(w), dtype=torch.int32, device="cuda")
+    tout = torch.empty_like(empty)
+    plan = torch.empty((S, w.K, 2), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((S,), dtype=torch.int32, device="cuda")
+    okv.oasis_select_topk_capped(scores, w.Nb, sl, w.B, w.Hkv, w.K, w.W, w.K, empty, tout, plan, cnt, lay.status)
+    t = tout.cpu()
+    rows = [wl.prior_from_topk(w, 0, s, [b for b in t[s, :w.K].tolist() if b >= 0]) for s in range(S)]
+    return torch.stack(rows)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_kv_cache_quest_gb300 as okv
+    from synth import workload as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    okv.load()
+    w = wl.WORKLOADS[WORKLOAD_ID]
+    dev = torch.device("cuda", local)
+
+    # ---- setup (untimed): KV cache, summaries, prior tables, pool, pinned host tier
+    tiles = torch.empty((w.S, w.Nb, 2, 16, w.D), dtype=torch.bfloat16, device=dev)
+    for s0 in range(0, w.S, 8):
+        tiles[s0:s0 + 8] = wl.kv_tiles(w, 0, list(range(s0, min(w.S, s0 + 8))), device=dev)
+    host = torch.empty(tiles.shape, dtype=torch.bfloat16).pin_memory()
+    host.copy_(tiles)
+    sl = wl.seq_lens(w).to(dev)
+    q = wl.q_true(w, 0).to(dev)
+    qd = wl.drafts(w, 0).to(dev)
+    shape = okv.LayerShape(B=w.B, Hkv=w.Hkv, G=w.G, D=w.D, Nb_max=w.Nb, K=w.K, W=w.W, cap=w.cap, Nd=w.Nd)
+    insts = []
+    strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
+    for i in range(args.rotate):
+        lay = okv.DecodeLayer(shape, device=dev)
+        lay.build_summary(tiles, sl, 0, w.Nb, strides=strides)
+        insts.append(lay)
+    table0 = _gpu_prior(w, insts[0], tiles, sl, q).to(dev)
+    idx = table0.long().clamp(min=0)
+    pool0 = tiles[torch.arange(w.S, device=dev)[:, None], idx]
+    for lay in insts:
+        lay.table.copy_(table0)
+        lay.pool.copy_(pool0)
+    new_keys = tiles[:, w.Nb - 1:w.Nb, 0]                  # keys of the newest block, [S][1][16][D]
+    streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    seg_stride = host[0].numel() * 2
+    torch.cuda.synchronize()
+    del pool0
+
+    def step(i, timers=None):
+        insts[i % len(insts)].step(q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
+                                   streams=streams, advance=False, timers=timers)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    timers = {}
+    clocks = ClockSampler(local) if rank == 0 else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record()
+    for i in range(args.steps):
+        step(i, timers)
+    e1.record()
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert insts[0].status.item() == 0, okv.strerror(insts[0].status.item())
+
+    kern = {}
+    for name, pairs in timers.items():
+        kern[name] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) * 1e3   # us
+    per_layer = w.headline_bytes_per_layer()
+    value = per_layer * world / (ms / 1e3) / 1e9
+    peak, peak_kind = _peaks()
+    score_bytes = w.summary_bytes_per_layer()
+    attn_bytes = w.kv_bytes_per_layer() + w.out_bytes_per_layer()
+    k_gbs = {"score": score_bytes / (kern["score"] * 1e-6) / 1e9, "attn": attn_bytes / (kern["attn"] * 1e-6) / 1e9}
+    dom = "attn" if kern["attn"] >= kern["score"] else "score"
+    roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": "k_score (oasis_score_blocks)"}[dom],
+            "bound": "hbm", "achieved": k_gbs[dom], "peak": peak, "unit": "GB/s", "frac": k_gbs[dom] / peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+            "traffic": None,
+            "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes,
+            "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak} for k in k_gbs if k != dom}}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, streams, world, dev)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": _config(w, {"l2": f"{len(insts)} rotating buffer sets "
+                                            f"({len(insts) * per_layer / 1e6:.0f} MB of step inputs > L2)",
+                                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+                "roofline": roof, "kernels_us": kern, "gpu_launches": 5 * args.steps,
+                "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, streams, world, dev):
+    """Same metric through the public step call with host buffers: H2D of the
+    step's inputs (queries, drafts, lengths, newest block's keys) from pinned
+    memory and D2H of its results (outputs, lse, new table, plan, counts)."""
+    import torch
+    import torch.distributed as dist
+    q_h = q.cpu().pin_memory()
+    qd_h = qd.cpu().pin_memory()
+    sl_h = sl.cpu().pin_memory()
+    nk_h = new_keys.contiguous().cpu().pin_memory()
+    q_d, qd_d, sl_d = torch.empty_like(q), torch.empty_like(qd), torch.empty_like(sl)
+    nk_d = torch.empty(nk_h.shape, dtype=nk_h.dtype, device=dev)
+    lay0 = insts[0]
+    outs = [(torch.empty(lay.out.shape, dtype=torch.float32).pin_memory(),
+             torch.empty(lay.lse.shape, dtype=torch.float32).pin_memory(),
+             torch.empty(lay.table_next.shape, dtype=torch.int32).pin_memory(),
+             torch.empty(lay.plan.shape, dtype=torch.int32).pin_memory(),
+             torch.empty(lay.plan_count.shape, dtype=torch.int32).pin_memory()) for lay in insts]
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, qd_h, sl_h, nk_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs[0])
+
+    def step(i):
+        lay = insts[i % len(insts)]
+        q_d.copy_(q_h, non_blocking=True)
+        qd_d.copy_(qd_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        nk_d.copy_(nk_h, non_blocking=True)
+        lay.step(q_d, qd_d, sl_d, host, seg_stride, w.Nb, new_keys=nk_d, new_block=w.Nb - 1, streams=streams,
+                 advance=False)
+        o = outs[i % len(insts)]
+        for dst, src in zip(o, (lay.out, lay.lse, lay.table_next, lay.plan, lay.plan_count)):
+            dst.copy_(src, non_blocking=True)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": w.headline_bytes_per_layer() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * oasis.h - C ABI of liboasis.so: the lookahead sparse decode hot path of
+ * OasisKV on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [XR] "OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead
+ *        Sparse Prefetching", paper review on xllm-io.github.io: §2 core idea,
+ *        §3 architecture (Fig. 5, eqs. (1)-(4), component table, decode flow),
+ *        §4 innovations (Figs. 6-9), §5 implementation, §6 experiments.
+ *   [LP] "Scaling KV Cache Beyond Memory Limits", legiblepapers.com: Key
+ *        Takeaways, FAQ Q4 and Q7.
+ *
+ * One decode step of one layer, per KV head ("segment" s = b * Hkv + h of
+ * sequence b and KV head h):
+ *   oasis_build_summary       per-block min/max key summaries (update path)
+ *   oasis_score_blocks        draft queries scan the summaries -> block scores
+ *   oasis_select_topk_capped  top-K, capped admission, eviction, plan, table
+ *   oasis_stage_blocks        host-resident KV tiles -> HBM slots (the plan)
+ *   oasis_sparse_decode_attn  attention of the true query over the slots
+ *
+ * Conventions shared by every entry point
+ *   Memory.     The caller allocates and owns every buffer.  The library
+ *               allocates no memory and keeps no state between calls (it only
+ *               caches, per process, that each kernel's shared-memory limit
+ *               was raised).  Device pointers must be device memory or, where
+ *               stated, host memory the GPU can address (pinned and mapped).
+ *   Execution.  Every call enqueues kernels on `stream` (NULL = the legacy
+ *               default stream) and returns without synchronising.  Outputs
+ *               are valid once the stream reaches that point.
+ *   Errors.     OASIS_EINVAL: an argument failed host-side validation; nothing
+ *               was launched.  OASIS_ECUDA: a launch failed (the CUDA error is
+ *               left for cudaGetLastError to report).  Faults that only the
+ *               device can see (an invalid table, a NaN score, a plan entry
+ *               out of range, a sequence longer than the summary capacity) are
+ *               OR-ed into the caller's int32 status word as OASIS_STATUS_*
+ *               bits; kernels never trap or assert.  The library never clears
+ *               the status word; pass NULL where the call allows it to skip
+ *               reporting.
+ *   Types.      bf16 is passed as uint16_t (the bit pattern of __nv_bfloat16);
+ *               fp32 as float; block ids and slots as int32_t.
+ *   Blocks.     A logical block holds 16 consecutive tokens; token t of block
+ *               b of sequence i is valid when 16*b + t < seq_len[i]
+ *               ([XR] §6 default parameters: block size 16).
+ *
+ * Layouts (element counts; all arrays dense and row-major)
+ *   KV tile     [2][16][D] bf16: the block's 16 keys, then its 16 values.
+ *               8 KiB at D = 128.  Both the host copy of the full cache and
+ *               the HBM slot pool are arrays of tiles.
+ *   pool        [S][slots_per_seg][2][16][D] bf16, slots_per_seg = K + W.
+ *   summary     kmin, kmax: [S][D/8][Nb_max][8] bf16 each ("chunk-major":
+ *               the 8 dims d = 8c .. 8c+7 of consecutive blocks are
+ *               consecutive in memory).
+ *   table       [S][K + W] int32: slot -> logical block id, -1 = empty.  Slots
+ *               0..K-1 hold the selected blocks, K..K+W-1 the local window.
+ *   queries     q [B][Hq][D] bf16 and qdraft [B][Nd][Hq][D] bf16, Hq = Hkv*G;
+ *               query head h*G + g (g < G) belongs to KV head h.
+ */
+#ifndef OASIS_H
+#define OASIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without including the CUDA headers (it is this same type). */
+typedef struct CUstream_st *oasis_stream_t;
+
+#define OASIS_ABI_VERSION 1
+
+/* Return codes. */
+#define OASIS_OK 0
+#define OASIS_EINVAL (-1)
+#define OASIS_ECUDA (-2)
+
+/* Bits of the device status word. */
+#define OASIS_STATUS_TABLE_RANGE 1  /* a resident block is not a candidate (outside [0, nc)) */
+#define OASIS_STATUS_TABLE_DUP 2    /* a block is resident in two slots of one segment */
+#define OASIS_STATUS_NAN_SCORE 4    /* a candidate's score is NaN (it ranks below all numbers) */
+#define OASIS_STATUS_PLAN_RANGE 8   /* a plan entry names a block or slot out of range; skipped */
+#define OASIS_STATUS_SEQ_LEN 16     /* seq_len < 0 or beyond 16 * Nb_max; clamped */
+#define OASIS_STATUS_TIMEOUT 32     /* a bounded device wait gave up; the output is incomplete */
+
+/* One transfer of the plan: host block src_block -> pool slot dst_slot. */
+typedef struct {
+  int32_t src_block;
+  int32_t dst_slot;
+} oasis_xfer_t;
+
+/* Text of a return code or of one status bit. */
+const char *oasis_strerror(int code);
+
+/* OASIS_ABI_VERSION of the loaded library. */
+int oasis_abi_version(void);
+
+/*
+ * Min/max key summaries of blocks [blk_begin, blk_begin + blk_count) of every
+ * segment - the full build at sparsification (blk_begin = 0, blk_count =
+ * Nb_max) or the per-step update of the newest blocks.
+ * [XR] §3 component table "Compressed Key Cache" (per-dimension min/max per
+ * logical block, 1/16 of the full KV); §5 compressed-key update.
+ *
+ * k:        bf16 keys; key d of token t of block blk_begin + j of segment s is
+ *           k[s*seg_stride + j*blk_stride + t*tok_stride + d].  16-byte
+ *           aligned; the three strides (elements) non-negative multiples of 8.
+ *           A KV tile array (full cache or pool) has tok_stride = D,
+ *           blk_stride = 32*D.
+ * seq_len:  int32 [B] valid tokens per sequence (device).
+ * kmin/kmax: summary arrays (layout above), written for every block of the
+ *           range that holds a valid token; other entries are not touched.
+ * Per dim, over the block's valid tokens: kmin = IEEE minimum, kmax = IEEE
+ * maximum, with -0 below +0.  Exact (no rounding).  NaN keys: undefined.
+ * EINVAL: a NULL pointer, D not 64 or 128, B or Hkv < 1, Nb_max < 1,
+ * blk_begin < 0, blk_count < 0, blk_begin + blk_count > Nb_max, a misaligned
+ * pointer or stride.  status may be NULL.
+ */
+int oasis_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
+                        int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
+                        uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, oasis_stream_t stream);
+
+/*
+ * Look-ahead block scores: the draft queries of each KV head scan its
+ * summaries ([XR] §3 decode flow; §4 Fig. 7).
+ *
+ * scores[s][b], float32 [S][Nb_max], is written for the candidate blocks
+ * b < nc = ceil(seq_len/16) - W of segment s (the W newest blocks form the
+ * always-resident window and are not scored); other entries are not touched.
+ *   score = max over the G query heads of KV head h and the Nd drafts of
+ *           sum_{d = 0..D-1, in this order, from +0, fp32 round-to-nearest}
+ *               q_d * (q_d >= 0 ? kmax_d : kmin_d)
+ * (each term is an exact fp32 product of two bf16 values, so the result is
+ * reproducible bit for bit).
+ * EINVAL: a NULL or misaligned pointer, D not 64 or 128, G not in [1, 16],
+ * Nd < 1, G*Nd > 64, B or Hkv < 1, W < 0, Nb_max < 1.  status may be NULL.
+ */
+int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
+                       int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
+                       float *scores, int32_t *status, oasis_stream_t stream);
+
+/*
+ * Per-KV-head top-K with capped admission ([XR] §3 decode flow and component
+ * table "Capped Eviction Policy" and "Head-wise Mapping"; §4 innovations;
+ * [LP] FAQ Q7).  One segment, nc = ceil(seq_len/16) - W candidates:
+ *   T  = the first min(K, nc) candidates by (score desc, block id asc); -0
+ *        equals +0; a NaN score ranks below every number.
+ *   R  = the blocks in table_in slots 0..K-1 (-1 = empty slot).
+ *   A  = the first `cap` blocks of T that are not in R, in the same order.
+ *   R' = the first K of R and A in that order, empty slots ranking below every
+ *        block: empty slots are filled first (lowest slot first), then the
+ *        lowest-ranked residents are evicted.
+ *   A in ascending block id takes the freed slots in ascending order; all
+ *   other slots, and the window slots K..K+W-1, keep their entries.
+ * table_out [S][K+W] receives the new table (it may alias table_in).
+ * plan [S][cap] receives plan_count[s] = |A| entries in ascending dst_slot;
+ * entries past plan_count[s] are set to {-1, -1}.
+ * A table whose slots 0..K-1 hold a block outside [0, nc) or the same block
+ * twice sets OASIS_STATUS_TABLE_RANGE / _DUP: that segment's table passes
+ * through unchanged and its plan is empty.
+ * EINVAL: a NULL pointer (status may not be NULL), B or Hkv < 1, K not in
+ * [1, 1024], W not in [0, 256], cap not in [0, K], Nb_max not in [1, 32768].
+ */
+int oasis_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
+                             int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
+                             oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, oasis_stream_t stream);
+
+/*
+ * Carry out the transfer plan: copy each planned block's KV tile from the host
+ * tier into its HBM slot ([XR] §3 Fig. 5 KV transfer worker; decode flow
+ * "asynchronous transfer").  Meant for a side stream ordered by events.
+ *
+ * host_kv:  device-addressable pointer to pinned, mapped host memory (on a
+ *           unified-address system the host pointer of cudaHostAlloc memory);
+ *           the tile of block blk of segment s starts at byte
+ *           s*host_seg_stride_bytes + blk*(64*D).  16-byte aligned, stride a
+ *           multiple of 16.  host_nb: blocks per segment in the host copy.
+ * plan, plan_count: as written by oasis_select_topk_capped (cap per segment).
+ * pool:     [S][slots_per_seg][2][16][D] bf16; slot dst_slot of segment s
+ *           receives the tile; other slots are not touched.
+ * An entry with src_block outside [0, host_nb) or dst_slot outside
+ * [0, slots_per_seg) is skipped and sets OASIS_STATUS_PLAN_RANGE.
+ * EINVAL: a NULL or misaligned pointer (status may not be NULL), D not 64 or
+ * 128, B or Hkv < 1, cap < 0, host_nb < 1, slots_per_seg < 1.
+ */
+int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int host_nb,
+                       const oasis_xfer_t *plan, const int32_t *plan_count, int cap, int B, int Hkv, int D,
+                       uint16_t *pool, int slots_per_seg, int32_t *status, oasis_stream_t stream);
+
+/*
+ * Sparse paged decode attention of the true queries over each KV head's
+ * resident slots ([XR] §3 Fig. 5 foreground sparse attention; Fig. 9
+ * head-wise mapping).  For query head h*G + g of sequence b:
+ *   out = sum_i p_i v_i,  p = softmax_i(scale * q . k_i)
+ * over every valid token i of every slot whose table entry is >= 0.
+ * out: float32 [B][Hq][D].  lse (may be NULL): float32 [B][Hq], the natural
+ * log of sum_i exp(scale * q . k_i).  No valid token: out = 0, lse = -inf.
+ * fp32 accumulation; against a float64 evaluation the error is within 1e-2
+ * max-abs and 1e-3 relative L2 on N(0,1)-like bf16 data.
+ * EINVAL: a NULL or misaligned pointer, D not 64 or 128, G not in [1, 16],
+ * B or Hkv < 1, slots_per_seg not in [1, 4096].  status may be NULL.
+ */
+int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
+                             const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,
+                             float *out, float *lse, int32_t *status, oasis_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OASIS_H */

@@ -1,0 +1,11 @@
+"""GB300-native lookahead sparse decode hot path of OasisKV.
+
+The kernels live in liboasis.so (C ABI: include/oasis.h); ``binding`` wraps
+each entry point under the same name, ``layer`` chains them into one decode
+step of one layer on CUDA streams.  Build the library with ``build.build()``.
+"""
+from .binding import (  # noqa: F401
+    EXPORTS, OasisError, abi_version, load, oasis_build_summary, oasis_score_blocks,
+    oasis_select_topk_capped, oasis_sparse_decode_attn, oasis_stage_blocks, strerror,
+)
+from .layer import DecodeLayer, LayerShape  # noqa: F401

@@ -1,0 +1,333 @@
+// Per-KV-head top-K selection with capped admission, eviction, transfer plan
+// and head-wise table update.
+//
+// OasisKV paper review (xllm-io): §3 decode flow (predict top-K -> compare with
+// the resident set -> build the transfer plan), §3 component table ("Capped
+// Eviction Policy": at most C new blocks per head per step, fetch ratio 0.05;
+// "Head-wise Mapping": per-KV-head logical-to-logical table), §4 innovations
+// (only head-wise mapping entries change).  legiblepapers, FAQ Q7: the cap is
+// applied at the KV-selection stage.
+//
+// Rule (per segment; T = top-K, R = residents, A = admitted, R' = new set):
+//   T  = first min(K, nc) candidates by (score desc, block asc)
+//   A  = first `cap` blocks of T \ R in that order
+//   R' = first K of R u A, empty slots ranking below every block
+//   A in ascending id takes the freed slots (filled empties, then the slots of
+//   evicted residents) in ascending slot order.
+//
+// One CTA of 512 threads per segment, everything in shared memory:
+//  * scores -> order-preserving 32-bit keys (larger key = larger score; -0 is
+//    mapped to +0 so the two tie; NaN maps to 0, below -inf, and is flagged);
+//  * T by a 4-pass 8-bit MSB radix select of the K-th largest key (warp-
+//    aggregated shared-memory histograms), then ties at the threshold taken in
+//    ascending block order through a block-wide prefix count;
+//  * T, R as bitmaps; the small lists T\R and R\T are ranked by counting
+//    (O(n^2) over <= K entries, no sorting network, few barriers) with the
+//    unique 64-bit composite key (key << 32) | ~block.
+#include "common.cuh"
+
+namespace oasis {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+
+__device__ __forceinline__ uint32_t score_key(float f, bool &nan) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) {
+    nan = true;
+    return 0u;
+  }
+  if (u == 0x80000000u) u = 0u;  // -0 ties with +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ uint64_t composite(uint32_t key, int b) {
+  return (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(b));
+}
+__device__ __forceinline__ int composite_block(uint64_t c) {
+  return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(c & 0xFFFFFFFFu));
+}
+
+__device__ __forceinline__ bool bit(const uint32_t *bm, int b) { return (bm[b >> 5] >> (b & 31)) & 1u; }
+
+// Exclusive prefix sum of v over the CTA (all threads call it).
+__device__ int block_exclusive_scan(int v, int *warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = lane < kWarps ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    if (lane < kWarps) warp_tot[lane] = t;  // inclusive totals
+  }
+  __syncthreads();
+  const int before_warp = warp > 0 ? warp_tot[warp - 1] : 0;
+  const int r = before_warp + x - v;
+  __syncthreads();  // warp_tot may be reused by the caller
+  return r;
+}
+
+struct SelScalars {
+  int err;
+  int nN, nE, nF, nEmpty;
+  uint32_t digit;
+  int remaining;
+  int warp_tot[kWarps];
+};
+
+__global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ scores, int Nb_max,
+                                                     const int32_t *__restrict__ seq_len, int Hkv, int K, int W,
+                                                     int cap, const int32_t *table_in, int32_t *table_out,
+                                                     oasis_xfer_t *__restrict__ plan, int32_t *__restrict__ plan_count,
+                                                     int32_t *status) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ SelScalars sc;
+  __shared__ uint32_t hist[256];
+
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slots = K + W;
+  const int words = (Nb_max + 31) >> 5;
+
+  uint64_t *listN = reinterpret_cast<uint64_t *>(smraw);       // [K]
+  uint64_t *listE = listN + K;                                 // [K]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(listE + K);   // [Nb_max]
+  uint32_t *bmR = keys + Nb_max;                               // [words]
+  uint32_t *bmT = bmR + words;                                 // [words]
+  int32_t *tin = reinterpret_cast<int32_t *>(bmT + words);     // [slots]
+  int32_t *slotE = tin + slots;                                // [K]
+  int32_t *rankN = slotE + K;                                  // [K]
+  int32_t *aSorted = rankN + K;                                // [cap]
+  int32_t *fList = aSorted + cap;                              // [cap]
+  int32_t *fSorted = fList + cap;                              // [cap]
+
+  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status, tid == 0 && (s % Hkv) == 0);
+  const int nc = max(0, ceil_div(L, kBlockTokens) - W);
+
+  // 1. table, bitmaps, keys
+  for (int i = tid; i < slots; i += kThreads) tin[i] = table_in[static_cast<int64_t>(s) * slots + i];
+  for (int i = tid; i < words; i += kThreads) {
+    bmR[i] = 0u;
+    bmT[i] = 0u;
+  }
+  if (tid == 0) {
+    sc.err = 0;
+    sc.nN = sc.nE = sc.nF = sc.nEmpty = 0;
+  }
+  bool nan = false;
+  const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
+  for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
+  __syncthreads();
+  if (nan) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
+
+  // 2. residents: range and duplicate checks, R bitmap, empty count
+  for (int i = tid; i < K; i += kThreads) {
+    const int blk = tin[i];
+    if (blk == -1) {
+      atomicAdd(&sc.nEmpty, 1);
+    } else if (blk < 0 || blk >= nc) {
+      atomicOr(&sc.err, OASIS_STATUS_TABLE_RANGE);
+    } else {
+      const uint32_t m = 1u << (blk & 31);
+      if (atomicOr(&bmR[blk >> 5], m) & m) atomicOr(&sc.err, OASIS_STATUS_TABLE_DUP);
+    }
+  }
+  __syncthreads();
+  const int err = sc.err;
+  if (err & (OASIS_STATUS_TABLE_RANGE | OASIS_STATUS_TABLE_DUP)) {
+    for (int i = tid; i < slots; i += kThreads) table_out[static_cast<int64_t>(s) * slots + i] = tin[i];
+    for (int k = tid; k < cap; k += kThreads) plan[static_cast<int64_t>(s) * cap + k] = oasis_xfer_t{-1, -1};
+    if (tid == 0) {
+      plan_count[s] = 0;
+      report(status, err);
+    }
+    return;
+  }
+
+  // 3. T = top-K candidates
+  if (nc <= K) {
+    for (int b = tid; b < nc; b += kThreads) atomicOr(&bmT[b >> 5], 1u << (b & 31));
+  } else {
+    uint32_t prefix = 0u, pmask = 0u;
+    int remaining = K;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
+        const int b = b0 + lane;
+        int dig = -1;
+        if (b < nc) {
+          const uint32_t key = keys[b];
+          if ((key & pmask) == prefix) dig = static_cast<int>((key >> shift) & 0xFFu);
+        }
+        const unsigned grp = __match_any_sync(0xFFFFFFFFu, dig);
+        if (dig >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hist[dig], static_cast<uint32_t>(__popc(grp)));
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l owns bins 255-8l down to 248-8l (descending digit order)
+        uint32_t c[8];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          c[q] = hist[255 - 8 * lane - q];
+          sum += c[q];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t before = incl - sum;
+        if (before < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl) {
+          uint32_t cum = before;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (cum < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= cum + c[q]) {
+              sc.digit = static_cast<uint32_t>(255 - 8 * lane - q);
+              sc.remaining = remaining - static_cast<int>(cum);
+            }
+            cum += c[q];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= sc.digit << shift;
+      pmask |= 0xFFu << shift;
+      remaining = sc.remaining;
+    }
+    const uint32_t tau = prefix;
+    const int need = remaining;  // keys equal to tau to take, lowest block id first
+    const int per = ceil_div(nc, kThreads);
+    const int lo = min(nc, tid * per), hi = min(nc, lo + per);
+    int ties = 0;
+    for (int b = lo; b < hi; ++b) ties += keys[b] == tau;
+    int before = block_exclusive_scan(ties, sc.warp_tot);
+    for (int b = lo; b < hi; ++b) {
+      const uint32_t key = keys[b];
+      bool in = key > tau;
+      if (key == tau) {
+        in = before < need;
+        ++before;
+      }
+      if (in) atomicOr(&bmT[b >> 5], 1u << (b & 31));
+    }
+  }
+  __syncthreads();
+
+  // 4. lists: N = T \ R (candidates to admit), E = R \ T (residents that may go)
+  for (int b = tid; b < nc; b += kThreads) {
+    if (bit(bmT, b) && !bit(bmR, b)) {
+      const int e = atomicAdd(&sc.nN, 1);
+      if (e < K) listN[e] = composite(keys[b], b);
+    }
+  }
+  for (int i = tid; i < K; i += kThreads) {
+    const int blk = tin[i];
+    if (blk >= 0 && !bit(bmT, blk)) {
+      const int e = atomicAdd(&sc.nE, 1);
+      if (e < K) {
+        listE[e] = composite(keys[blk], blk);
+        slotE[e] = i;
+      }
+    }
+  }
+  __syncthreads();
+  const int nN = min(sc.nN, K), nE = min(sc.nE, K), nEmpty = sc.nEmpty;
+  const int nA = min(cap, nN);
+  const int nEvict = max(0, nA - nEmpty);
+  const int nFill = nA - nEvict;
+
+  // 5. A = the nA best of N; freed slots = first nFill empty slots + the nEvict worst of E
+  for (int i = tid; i < nN; i += kThreads) {
+    const uint64_t ci = listN[i];
+    int r = 0;
+    for (int j = 0; j < nN; ++j) r += listN[j] > ci;
+    rankN[i] = r;
+  }
+  for (int i = tid; i < nE; i += kThreads) {
+    const uint64_t ci = listE[i];
+    int r = 0;
+    for (int j = 0; j < nE; ++j) r += listE[j] < ci;
+    if (r < nEvict) {
+      const int f = atomicAdd(&sc.nF, 1);
+      if (f < cap) fList[f] = slotE[i];
+    }
+  }
+  for (int i = tid; i < K; i += kThreads) {
+    if (tin[i] == -1) {
+      int r = 0;
+      for (int j = 0; j < i; ++j) r += tin[j] == -1;
+      if (r < nFill) {
+        const int f = atomicAdd(&sc.nF, 1);
+        if (f < cap) fList[f] = i;
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < nN; i += kThreads) {
+    if (rankN[i] < nA) {
+      const int b = composite_block(listN[i]);
+      int r = 0;
+      for (int j = 0; j < nN; ++j) r += rankN[j] < nA && composite_block(listN[j]) < b;
+      if (r < cap) aSorted[r] = b;
+    }
+  }
+  for (int i = tid; i < nA; i += kThreads) {
+    const int sl = fList[i];
+    int r = 0;
+    for (int j = 0; j < nA; ++j) r += fList[j] < sl;
+    if (r < cap) fSorted[r] = sl;
+  }
+  __syncthreads();
+
+  // 6. outputs
+  for (int k = tid; k < nA; k += kThreads) {
+    const int sl = fSorted[k];
+    if (sl >= 0 && sl < K) tin[sl] = aSorted[k];
+  }
+  __syncthreads();
+  for (int i = tid; i < slots; i += kThreads) table_out[static_cast<int64_t>(s) * slots + i] = tin[i];
+  for (int k = tid; k < cap; k += kThreads)
+    plan[static_cast<int64_t>(s) * cap + k] = k < nA ? oasis_xfer_t{aSorted[k], fSorted[k]} : oasis_xfer_t{-1, -1};
+  if (tid == 0) {
+    plan_count[s] = nA;
+    report(status, err);
+  }
+}
+
+}  // namespace
+
+size_t select_smem_bytes(int Nb_max, int K, int W, int cap) {
+  const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
+  return 2 * sizeof(uint64_t) * K + sizeof(uint32_t) * (Nb_max + 2 * words) +
+         sizeof(int32_t) * (static_cast<size_t>(K + W) + 2 * K + 3 * static_cast<size_t>(cap));
+}
+
+cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
+                                      int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
+                                      oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st) {
+  const size_t smem = select_smem_bytes(Nb_max, K, W, cap);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k_select<<<B * Hkv, kThreads, smem, st>>>(scores, Nb_max, seq_len, Hkv, K, W, cap, table_in, table_out, plan,
+                                             plan_count, status);
+  return cudaGetLastError();
+}
+
+}  // namespace oasis

@@ -1,0 +1,86 @@
+// Min/max key summaries per 16-token block (Quest-style compressed key cache).
+//
+// OasisKV paper review (xllm-io), §3 component table "Compressed Key Cache":
+// every logical block keeps a per-dimension min/max of its keys, 1/16 of the
+// full KV; §5: compressed keys are updated during decode.
+//
+// One thread per (segment, block, 8-dim chunk): it reads the chunk's 16 bytes
+// from each valid token row (consecutive threads read consecutive chunks of a
+// row, so a warp reads whole 256-byte rows) and writes 16 bytes to kmin and
+// kmax in the chunk-major layout [S][D/8][Nb_max][8].
+//
+// min/max use the IEEE 754-2019 total order of non-NaN values (-0 below +0):
+// each bf16 bit pattern u maps to the 16-bit key u | 0x8000 (u >= +0) or ~u
+// (u negative), which is monotone in value, so unsigned min/max of keys picks
+// the IEEE minimum/maximum exactly.  Two halves of a 32-bit word are handled
+// at once with the SIMD-within-a-word intrinsics __vminu2 / __vmaxu2.
+#include "common.cuh"
+
+namespace oasis {
+namespace {
+
+__device__ __forceinline__ uint32_t to_key2(uint32_t w) {
+  const uint32_t neg = (w >> 15) & 0x00010001u;
+  return w ^ ((neg * 0x7FFFu) | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t from_key2(uint32_t k) {
+  const uint32_t neg = ((~k) >> 15) & 0x00010001u;
+  return k ^ ((neg * 0x7FFFu) | 0x80008000u);
+}
+
+__global__ void __launch_bounds__(256) k_build_summary(const uint16_t *__restrict__ k, int64_t seg_stride,
+                                                       int64_t blk_stride, int64_t tok_stride, int Hkv, int D,
+                                                       const int32_t *__restrict__ seq_len, int blk_begin,
+                                                       int blk_count, uint16_t *__restrict__ kmin,
+                                                       uint16_t *__restrict__ kmax, int Nb_max,
+                                                       int32_t *status) {
+  const int s = blockIdx.y;
+  const int chunks = D >> 3;
+  const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status,
+                         blockIdx.x == 0 && threadIdx.x == 0 && (s % Hkv) == 0);
+  if (item >= static_cast<int64_t>(blk_count) * chunks) return;
+  const int j = static_cast<int>(item / chunks);
+  const int c = static_cast<int>(item % chunks);
+  const int b = blk_begin + j;
+  const int nvalid = min(kBlockTokens, L - kBlockTokens * b);
+  if (nvalid <= 0) return;
+
+  const uint16_t *p = k + s * seg_stride + j * blk_stride + c * 8;
+  uint4 lo = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
+  uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 4
+  for (int t = 0; t < nvalid; ++t) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p + t * tok_stride));
+    const uint32_t a = to_key2(v.x), bb = to_key2(v.y), cc = to_key2(v.z), dd = to_key2(v.w);
+    lo.x = __vminu2(lo.x, a);
+    lo.y = __vminu2(lo.y, bb);
+    lo.z = __vminu2(lo.z, cc);
+    lo.w = __vminu2(lo.w, dd);
+    hi.x = __vmaxu2(hi.x, a);
+    hi.y = __vmaxu2(hi.y, bb);
+    hi.z = __vmaxu2(hi.z, cc);
+    hi.w = __vmaxu2(hi.w, dd);
+  }
+  const int64_t o = ((static_cast<int64_t>(s) * chunks + c) * Nb_max + b) * 8;
+  *reinterpret_cast<uint4 *>(kmin + o) =
+      make_uint4(from_key2(lo.x), from_key2(lo.y), from_key2(lo.z), from_key2(lo.w));
+  *reinterpret_cast<uint4 *>(kmax + o) =
+      make_uint4(from_key2(hi.x), from_key2(hi.y), from_key2(hi.z), from_key2(hi.w));
+}
+
+}  // namespace
+
+cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
+                                 int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
+                                 uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, cudaStream_t st) {
+  const int S = B * Hkv;
+  const int64_t items = static_cast<int64_t>(blk_count) * (D / 8);
+  const int threads = 256;
+  const dim3 grid(static_cast<unsigned>((items + threads - 1) / threads), static_cast<unsigned>(S));
+  k_build_summary<<<grid, threads, 0, st>>>(k, seg_stride, blk_stride, tok_stride, Hkv, D, seq_len, blk_begin,
+                                            blk_count, kmin, kmax, Nb_max, status);
+  return cudaGetLastError();
+}
+
+}  // namespace oasis

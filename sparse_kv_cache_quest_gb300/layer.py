@@ -1,0 +1,157 @@
+"""Per-layer device state and one decode step, built on the C ABI.
+
+This is orchestration only (buffers, streams, events, argument marshalling):
+every step of the path runs in liboasis.so's kernels.
+
+Step order, after the OasisKV paper review (xllm-io), §3 decode flow and
+Fig. 8 (asynchronous prefetch pipeline): the foreground attends the true
+query over the blocks resident now, while the background scores the blocks
+with the draft queries and selects the next resident set; the transfer of the
+admitted blocks starts once both are done (the slots it overwrites may still
+be read by the attention of this step) and must finish before the next
+step's attention.  Foreground and background run on separate CUDA streams
+ordered by events ([XR] §5).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import binding as ob
+
+BLOCK = 16
+
+
+@dataclass
+class LayerShape:
+    B: int
+    Hkv: int
+    G: int
+    D: int
+    Nb_max: int
+    K: int
+    W: int
+    cap: int
+    Nd: int
+
+    @property
+    def S(self) -> int:
+        return self.B * self.Hkv
+
+    @property
+    def Hq(self) -> int:
+        return self.Hkv * self.G
+
+    @property
+    def slots(self) -> int:
+        return self.K + self.W
+
+
+class DecodeLayer:
+    """Device buffers of one layer: summaries, scores, tables, plan, pool, outputs."""
+
+    def __init__(self, shape: LayerShape, device="cuda"):
+        self.shape = sh = shape
+        dev = torch.device(device)
+        self.device = dev
+        self.kmin = torch.zeros((sh.S, sh.D // 8, sh.Nb_max, 8), dtype=torch.bfloat16, device=dev)
+        self.kmax = torch.zeros_like(self.kmin)
+        self.scores = torch.zeros((sh.S, sh.Nb_max), dtype=torch.float32, device=dev)
+        self.table = torch.full((sh.S, sh.slots), -1, dtype=torch.int32, device=dev)
+        self.table_next = torch.full_like(self.table, -1)
+        self.plan = torch.full((sh.S, max(sh.cap, 1), 2), -1, dtype=torch.int32, device=dev)
+        self.plan_count = torch.zeros((sh.S,), dtype=torch.int32, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        self.pool = torch.zeros((sh.S, sh.slots, 2, BLOCK, sh.D), dtype=torch.bfloat16, device=dev)
+        self.out = torch.zeros((sh.B, sh.Hq, sh.D), dtype=torch.float32, device=dev)
+        self.lse = torch.zeros((sh.B, sh.Hq), dtype=torch.float32, device=dev)
+        self.scale = 1.0 / math.sqrt(sh.D)
+
+    # -- individual steps ---------------------------------------------------
+    def build_summary(self, keys, seq_len, blk_begin=0, blk_count=None, strides=None, stream=None):
+        """keys: bf16 [S][n][16][D] (or a tile array [S][n][2][16][D] with strides) of blocks
+        blk_begin .. blk_begin + n - 1."""
+        sh = self.shape
+        if strides is None:
+            seg, blk, tok = keys.stride(0), keys.stride(1), keys.stride(-2)
+        else:
+            seg, blk, tok = strides
+        n = keys.shape[1] if blk_count is None else blk_count
+        ob.oasis_build_summary(keys, seg, blk, tok, sh.B, sh.Hkv, sh.D, seq_len, blk_begin, n,
+                               self.kmin, self.kmax, sh.Nb_max, self.status, stream)
+
+    def score(self, qdraft, seq_len, stream=None):
+        sh = self.shape
+        ob.oasis_score_blocks(self.kmin, self.kmax, sh.Nb_max, qdraft, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D,
+                              seq_len, sh.W, self.scores, self.status, stream)
+
+    def select(self, seq_len, stream=None):
+        sh = self.shape
+        ob.oasis_select_topk_capped(self.scores, sh.Nb_max, seq_len, sh.B, sh.Hkv, sh.K, sh.W, sh.cap,
+                                    self.table, self.table_next, self.plan, self.plan_count, self.status, stream)
+
+    def stage(self, host_kv, host_seg_stride_bytes, host_nb, stream=None):
+        sh = self.shape
+        ob.oasis_stage_blocks(host_kv, host_seg_stride_bytes, host_nb, self.plan, self.plan_count, sh.cap,
+                              sh.B, sh.Hkv, sh.D, self.pool, sh.slots, self.status, stream)
+
+    def attend(self, q, seq_len, stream=None):
+        sh = self.shape
+        ob.oasis_sparse_decode_attn(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D,
+                                    self.scale, self.out, self.lse, self.status, stream)
+
+    def swap_tables(self):
+        self.table, self.table_next = self.table_next, self.table
+
+    # -- one decode step ----------------------------------------------------
+    def step(self, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
+             new_block: Optional[int] = None, streams=None, advance: bool = True, timers=None):
+        """One decode step of this layer; returns (out, lse) of the attention.
+
+        new_keys (optional): bf16 [S][1][16][D] keys of block ``new_block`` whose
+        summary is refreshed first (the compressed-key update of a decode step).
+        streams: (foreground, background, transfer) CUDA streams; the current
+        stream for all three when None.  The caller's current stream is made
+        to wait for the whole step.
+        advance: make the new table current (False keeps the old table current,
+        so repeated steps start from the same resident set).
+        timers: optional dict; CUDA event pairs around the attention ("attn",
+        foreground stream) and the scoring ("score", background stream) are
+        appended to timers[name].
+        """
+        cur = torch.cuda.current_stream(self.device)
+        fg, bg, xf = streams if streams is not None else (cur, cur, cur)
+        start = torch.cuda.Event()
+        start.record(cur)
+        for s_ in (fg, bg, xf):
+            s_.wait_event(start)
+        if new_keys is not None:
+            self.build_summary(new_keys, seq_len, blk_begin=new_block, blk_count=1, stream=bg)
+        def timed(name, st, fn):
+            if timers is None:
+                fn()
+                return
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            timers.setdefault(name, []).append((a, b))
+
+        timed("attn", fg, lambda: self.attend(q, seq_len, stream=fg))
+        timed("score", bg, lambda: self.score(qdraft, seq_len, stream=bg))
+        timed("select", bg, lambda: self.select(seq_len, stream=bg))
+        e_fg, e_bg = torch.cuda.Event(), torch.cuda.Event()
+        e_fg.record(fg)
+        e_bg.record(bg)
+        xf.wait_event(e_fg)
+        xf.wait_event(e_bg)
+        timed("stage", xf, lambda: self.stage(host_kv, host_seg_stride_bytes, host_nb, stream=xf))
+        done = torch.cuda.Event()
+        done.record(xf)
+        cur.wait_event(done)
+        if advance:
+            self.swap_tables()
+        return self.out, self.lse

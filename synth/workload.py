@@ -275,6 +275,7 @@ def prior_from_topk(w: Workload, layer: int, s: int, topk: list[int], keep_frac:
     kept and the rest of the K slots get random candidates outside ``topk``;
     slots hold the blocks in ascending order, followed by the window blocks.
     """
+    topk = sorted(int(b) for b in topk)
     k = len(topk)
     keep = int(Fraction(keep_frac) * k + Fraction(1, 2))
     off = (layer * w.S + s) * w.Nb
