@@ -40,7 +40,7 @@ WORKLOAD_ID = 2
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=8000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--rotate", type=int, default=4, help="independent buffer sets cycled to defeat L2")
@@ -77,23 +77,34 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index=0):
-        self.proc = None
+        import shutil
+        import threading
+        self.proc, self.lines = None, []
+        cmd = ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if shutil.which("stdbuf"):
+            cmd = ["stdbuf", "-oL"] + cmd
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+            return
+        self.reader = threading.Thread(target=lambda: self.lines.extend(iter(self.proc.stdout.readline, "")),
+                                       daemon=True)
+        self.reader.start()
+        time.sleep(0.25)
 
     def stop(self):
         if self.proc is None:
             return None
+        time.sleep(0.15)
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.reader.join(timeout=5)
+        out = "".join(self.lines)
         sms, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -265,44 +276,74 @@ def run_ours(args):
     for lay in insts:
         lay.table.copy_(table0)
         lay.pool.copy_(pool0)
-    new_keys = tiles[:, w.Nb - 1:w.Nb, 0]                  # keys of the newest block, [S][1][16][D]
-    streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    new_keys = tiles[:, w.Nb - 1:w.Nb, 0].contiguous()     # keys of the newest block, [S][1][16][D]
     seg_stride = host[0].numel() * 2
     torch.cuda.synchronize()
     del pool0
 
-    def step(i, timers=None):
-        insts[i % len(insts)].step(q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
-                                   streams=streams, advance=False, timers=timers)
+    graphs = [okv.StepGraph(lay, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1)
+              for lay in insts]
+    R = len(graphs)
+    rounds = max(1, (args.steps + R - 1) // R)
+    steps = rounds * R
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
-        step(i)
+    for i in range(max(1, (args.warmup + R - 1) // R)):
+        for g in graphs:
+            g.replay()
     barrier()
-    timers = {}
     clocks = ClockSampler(local) if rank == 0 else None
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    torch.cuda.nvtx.range_push("oasis_timed")
     e0.record()
-    for i in range(args.steps):
-        step(i, timers)
+    for _ in range(rounds):
+        for g in graphs:
+            g.replay()
     e1.record()
+    torch.cuda.nvtx.range_pop()
     barrier()
     clk = clocks.stop() if clocks else None
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     assert insts[0].status.item() == 0, okv.strerror(insts[0].status.item())
 
+    # per-kernel durations: a CUDA graph of back-to-back launches of one kernel
+    # over the rotating buffer sets, replayed between events on the replay stream
     kern = {}
-    for name, pairs in timers.items():
-        kern[name] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs) * 1e3   # us
+    calls = {"score": lambda lay, st: lay.score(qd, sl, stream=st),
+             "attn": lambda lay, st: lay.attend(q, sl, stream=st),
+             "select": lambda lay, st: lay.select(sl, stream=st),
+             "stage": lambda lay, st: lay.stage(host, seg_stride, w.Nb, stream=st),
+             "summary_update": lambda lay, st: lay.build_summary(new_keys, sl, blk_begin=w.Nb - 1, blk_count=1,
+                                                                 stream=st)}
+    n_launch = 4 * R
+    for name, fn in calls.items():
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(kg, stream=side):
+            for i in range(n_launch):
+                fn(insts[i % R], side)
+        kg.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        torch.cuda.nvtx.range_push(f"oasis_kernel_{name}")
+        a.record()
+        for _ in range(reps):
+            kg.replay()
+        b.record()
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        kern[name] = a.elapsed_time(b) / (reps * n_launch) * 1e3      # us per launch
     per_layer = w.headline_bytes_per_layer()
     value = per_layer * world / (ms / 1e3) / 1e9
     peak, peak_kind = _peaks()
@@ -315,80 +356,63 @@ def run_ours(args):
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
             "traffic": None,
             "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes,
+            "timing": "CUDA graph of back-to-back launches over the rotating buffer sets, CUDA events",
             "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak} for k in k_gbs if k != dom}}
 
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, streams, world, dev)
+        e2e = _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = _cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
                 "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
                 "config": _config(w, {"l2": f"{len(insts)} rotating buffer sets "
                                             f"({len(insts) * per_layer / 1e6:.0f} MB of step inputs > L2)",
                                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-                "roofline": roof, "kernels_us": kern, "gpu_launches": 5 * args.steps,
+                "roofline": roof, "kernels_us": kern, "gpu_launches": 5 * steps,
                 "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, streams, world, dev):
-    """Same metric through the public step call with host buffers: H2D of the
-    step's inputs (queries, drafts, lengths, newest block's keys) from pinned
-    memory and D2H of its results (outputs, lse, new table, plan, counts)."""
+def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev):
+    """Same metric through the public step call with host buffers: every step
+    is one StepGraph replay that copies the step's inputs (queries, drafts,
+    lengths, newest block's keys) from pinned host memory, runs the step and
+    copies its results (outputs, lse, new table, plan, counts) back."""
     import torch
     import torch.distributed as dist
-    q_h = q.cpu().pin_memory()
-    qd_h = qd.cpu().pin_memory()
-    sl_h = sl.cpu().pin_memory()
-    nk_h = new_keys.contiguous().cpu().pin_memory()
-    q_d, qd_d, sl_d = torch.empty_like(q), torch.empty_like(qd), torch.empty_like(sl)
-    nk_d = torch.empty(nk_h.shape, dtype=nk_h.dtype, device=dev)
-    lay0 = insts[0]
-    outs = [(torch.empty(lay.out.shape, dtype=torch.float32).pin_memory(),
-             torch.empty(lay.lse.shape, dtype=torch.float32).pin_memory(),
-             torch.empty(lay.table_next.shape, dtype=torch.int32).pin_memory(),
-             torch.empty(lay.plan.shape, dtype=torch.int32).pin_memory(),
-             torch.empty(lay.plan_count.shape, dtype=torch.int32).pin_memory()) for lay in insts]
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, qd_h, sl_h, nk_h))
-    d2h = sum(t.numel() * t.element_size() for t in outs[0])
 
-    def step(i):
-        lay = insts[i % len(insts)]
-        q_d.copy_(q_h, non_blocking=True)
-        qd_d.copy_(qd_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        nk_d.copy_(nk_h, non_blocking=True)
-        lay.step(q_d, qd_d, sl_d, host, seg_stride, w.Nb, new_keys=nk_d, new_block=w.Nb - 1, streams=streams,
-                 advance=False)
-        o = outs[i % len(insts)]
-        for dst, src in zip(o, (lay.out, lay.lse, lay.table_next, lay.plan, lay.plan_count)):
-            dst.copy_(src, non_blocking=True)
-
-    for i in range(args.warmup):
-        step(i)
+    import sparse_kv_cache_quest_gb300 as okv
+    graphs = [okv.StepGraph(lay, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
+                            host_io=True) for lay in insts]
+    R = len(graphs)
+    rounds = max(1, (args.steps + R - 1) // R)
+    for g in graphs:
+        g.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(args.steps):
-        step(i)
+    for _ in range(rounds):
+        for g in graphs:
+            g.replay()
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = e0.elapsed_time(e1) / (rounds * R)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return {"value": w.headline_bytes_per_layer() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": graphs[0].h2d_bytes, "d2h_bytes_per_step": graphs[0].d2h_bytes,
+            "how": "StepGraph(host_io=True).replay(): H2D inputs + step + D2H results per step"}
 
 
 def main():

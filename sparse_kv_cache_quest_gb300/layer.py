@@ -155,3 +155,55 @@ class DecodeLayer:
         if advance:
             self.swap_tables()
         return self.out, self.lse
+
+
+class StepGraph:
+    """One decode step of a DecodeLayer captured as a CUDA graph.
+
+    The graph reads its inputs from static device buffers owned by this object
+    (copy new values into ``q``, ``qdraft``, ``seq_len``, ``new_keys`` or, with
+    host_io=True, into the pinned host staging tensors ``host_in``) and writes
+    the layer's outputs; ``replay()`` runs the whole step - and with host_io,
+    the host->device copies of the step's inputs and the device->host copies
+    of its results (out, lse, new table, plan, plan counts into ``host_out``) -
+    as one graph launch, without per-kernel launch overhead.  The step keeps
+    the layer's current table (the new table is left in ``layer.table_next``).
+    """
+
+    def __init__(self, layer: DecodeLayer, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb,
+                 new_keys=None, new_block: Optional[int] = None, host_io: bool = False):
+        dev = layer.device
+        self.layer = layer
+        self.q = q.detach().to(dev).clone()
+        self.qdraft = qdraft.detach().to(dev).clone()
+        self.seq_len = seq_len.detach().to(dev).clone()
+        self.new_keys = new_keys.detach().to(dev).contiguous().clone() if new_keys is not None else None
+        ins = [self.q, self.qdraft, self.seq_len] + ([self.new_keys] if self.new_keys is not None else [])
+        outs = [layer.out, layer.lse, layer.table_next, layer.plan, layer.plan_count]
+        self.host_in = [t.cpu().pin_memory() for t in ins] if host_io else []
+        self.host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] if host_io else []
+        self.streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        args = (host_kv, host_seg_stride_bytes, host_nb)
+
+        def body():
+            for d, h in zip(ins, self.host_in):
+                d.copy_(h, non_blocking=True)
+            layer.step(self.q, self.qdraft, self.seq_len, *args, new_keys=self.new_keys, new_block=new_block,
+                       streams=self.streams, advance=False)
+            for h, d in zip(self.host_out, outs):
+                h.copy_(d, non_blocking=True)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body()                                   # warm-up outside capture (lazy initialisation)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            body()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in self.host_out)
+
+    def replay(self):
+        self.graph.replay()
