@@ -1,6 +1,8 @@
 // extern "C" entry points of liboasis.so: host-side argument validation, then
 // one launch each.  Declared and documented in include/oasis.h.
 #include <cstdint>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 
@@ -15,6 +17,49 @@ inline bool segs_ok(int B, int Hkv) {
 inline int finish(cudaError_t e) { return e == cudaSuccess ? OASIS_OK : OASIS_ECUDA; }
 
 }  // namespace
+
+namespace oasis {
+
+// SM count and resident CTAs per SM of a kernel at a given dynamic shared-memory
+// size, after raising the kernel's shared-memory limit to that size.  Cached
+// per process, device, kernel, block size and shared-memory size.
+cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm) {
+  struct Entry {
+    const void *fn;
+    int dev, threads;
+    size_t smem;
+    int sms, per_sm;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry &x : cache)
+      if (x.fn == fn && x.dev == dev && x.threads == threads && x.smem == smem) {
+        *sms = x.sms;
+        *per_sm = x.per_sm;
+        return cudaSuccess;
+      }
+  }
+  int n = 0, p = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p, fn, threads, smem);
+  if (e != cudaSuccess) return e;
+  p = p < 1 ? 1 : p;
+  std::lock_guard<std::mutex> lk(mu);
+  cache.push_back(Entry{fn, dev, threads, smem, n, p});
+  *sms = n;
+  *per_sm = p;
+  return cudaSuccess;
+}
+
+}  // namespace oasis
 
 extern "C" {
 

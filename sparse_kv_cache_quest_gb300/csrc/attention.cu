@@ -12,23 +12,33 @@
 // (split-K): CTA rank r takes a contiguous slot range, and inside it warp w
 // takes every 4th slot.  Each warp streams its tiles through a private ring of
 // NST shared-memory stages with 1-D bulk async copies (cp.async.bulk, one
-// mbarrier per stage, lane 0 issues), so up to NST tiles per warp are in
-// flight.  Empty slots and slots without valid tokens are never loaded.
+// mbarrier per stage, lane 0 issues), so the next tile is in flight while one
+// is consumed.  Empty slots and slots without valid tokens are never loaded.
 //
-// Math.  A warp works on one 16-token slot at a time: lane (tsub, dpart) owns
-// dims dpart*VEC .. dpart*VEC + VEC - 1 of tokens 2u + tsub (u < 8).  Partial
-// dots are summed over the 16 lanes of a half with xor shuffles; the online
-// softmax runs in the log2 domain (q is pre-multiplied by scale * log2(e),
-// exp2f), with per-warp running max m, sum l and output o[g][dims] in fp32.
-// Warps combine through shared memory, then the CL CTAs of the cluster
-// combine through distributed shared memory into rank 0, which writes out and
-// lse.  No global scratch memory is used.
+// Math (CUDA cores: a GQA group of a few heads is no dense tensor-core tile).
+// A warp works on one 16-token slot at a time.  Lane (tsub = lane/16,
+// dpart = lane%16) owns dims dpart*VEC .. +VEC of tokens 2u + tsub (u < 8).
+//  * QK: per lane, partial dots of its dims for its 8 tokens and the GT query
+//    heads, two heads per packed fp32x2 FMA.  The lane visits its tokens in the
+//    order u_i = i ^ rot (rot = dpart bits 3..1) and holds its heads in the
+//    order g_k = k ^ (dpart bit 0) * GT/2, so that a butterfly reduce-scatter
+//    over the 16 lanes of a half (xor 8, 4, 2 over tokens, xor 1 over heads)
+//    always exchanges registers with static indices (GT*7 + GT/2 shuffles
+//    instead of an all-reduce's 32*GT); afterwards each lane owns the complete
+//    logits of token 2*rot + tsub for heads g_0 .. g_{GT/2-1}.
+//  * Online softmax in the log2 domain (q pre-scaled by scale*log2(e), exp2f)
+//    on the owned logits only; running max m and sum l per head.
+//  * PV: each lane gathers p for its 8 tokens and GT heads with shuffles and
+//    accumulates o[g][its dims] with packed fp32x2 FMAs over dim pairs.
+// Warps combine through shared memory (reusing the rings), then the CL CTAs of
+// the cluster combine through distributed shared memory into rank 0, which
+// writes out and lse.  No global scratch memory is used.
 //
 // G > 8 is processed in query-head tiles of 8 (separate clusters).
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <cfloat>
-#include <cstdlib>
 
 #include "common.cuh"
 
@@ -42,6 +52,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kWaitTries = 1u << 22;  // bounded mbarrier polls (far beyond any real copy)
 constexpr float kLn2 = 0.69314718055994530942f;
 
+// Widen VEC bf16 (16 or 8 bytes of shared memory) to fp32.
 template <int VEC>
 __device__ __forceinline__ void load_row(const uint16_t *p, float (&f)[VEC]) {
   if constexpr (VEC == 8) {
@@ -54,18 +65,32 @@ __device__ __forceinline__ void load_row(const uint16_t *p, float (&f)[VEC]) {
   }
 }
 
+template <int VEC, int GT>
+struct Smem {
+  static constexpr int D = 16 * VEC;
+  static constexpr int kTile = 64 * D;  // bytes per slot tile
+  // combine scratch (floats), aliased onto the rings after the main loop
+  static constexpr int kWarpM = 0, kWarpL = kWarps * GT, kWarpO = 2 * kWarps * GT;
+  static constexpr int kCtaM = kWarpO + kWarps * GT * D, kCtaL = kCtaM + GT, kCtaO = kCtaL + GT;
+  static constexpr int kScratchFloats = kCtaO + GT * D;
+};
+
 template <int VEC, int GT, int NST>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
     k_attn(const uint16_t *__restrict__ q, const uint16_t *__restrict__ pool, const int32_t *__restrict__ table,
            int slots, const int32_t *__restrict__ seq_len, int Hkv, int G, int ntiles, float scale_log2,
            float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
-  constexpr int D = 16 * VEC;
-  constexpr uint32_t kTileBytes = 64u * D;
+  using SM = Smem<VEC, GT>;
+  constexpr int D = SM::D;
+  constexpr uint32_t kTileBytes = SM::kTile;
+  constexpr int H = GT > 1 ? GT / 2 : 1;  // heads owned per lane after the reduce-scatter
   extern __shared__ __align__(128) unsigned char sm[];
   cg::cluster_group cluster = cg::this_cluster();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tsub = lane >> 4, dpart = lane & 15;
+  const int rot = (dpart >> 1) & 7;  // token order u_i = i ^ rot
+  const int hb = dpart & 1;          // head order  g_k = k ^ hb * GT/2
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
   const int s = blockIdx.y / ntiles, tile = blockIdx.y % ntiles;
@@ -82,14 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   unsigned char *ring = sm + static_cast<size_t>(warp) * NST * kTileBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + static_cast<size_t>(kWarps) * NST * kTileBytes) + warp * NST;
-  float *red = reinterpret_cast<float *>(sm + static_cast<size_t>(kWarps) * NST * kTileBytes +
-                                         sizeof(uint64_t) * kWarps * NST);
-  float *wm = red;                          // [kWarps][GT]
-  float *wl = wm + kWarps * GT;             // [kWarps][GT]
-  float *wo = wl + kWarps * GT;             // [kWarps][GT][D]
-  float *cm = wo + kWarps * GT * D;         // [GT]   CTA partials, read by cluster rank 0
-  float *cl = cm + GT;                      // [GT]
-  float *co = cl + GT;                      // [GT][D]
+  float *scratch = reinterpret_cast<float *>(sm);  // used only once every ring stage is drained
 
   if (lane == 0) {
     for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
@@ -97,28 +115,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // queries of this lane's dims, pre-scaled into the log2 domain
-  float qr[GT][VEC];
+  // query slot k holds head g_k = k ^ (hb * GT/2); packed in head pairs for fp32x2
+  unsigned long long q2[(GT + 1) / 2][VEC];
+  {
+    float qf[GT][VEC];
 #pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    if (g < gcount) {
-      float f[VEC];
-      load_row<VEC>(q + (static_cast<int64_t>(bseq) * Hq + h * G + g0 + g) * D + dpart * VEC, f);
+    for (int k = 0; k < GT; ++k) {
+      const int g = GT > 1 ? (k ^ (hb * (GT / 2))) : 0;
+      if (g < gcount) {
+        float f[VEC];
+        load_row<VEC>(q + (static_cast<int64_t>(bseq) * Hq + h * G + g0 + g) * D + dpart * VEC, f);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) qr[g][e] = f[e] * scale_log2;
-    } else {
+        for (int e = 0; e < VEC; ++e) qf[k][e] = f[e] * scale_log2;
+      } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) qr[g][e] = 0.0f;
+        for (int e = 0; e < VEC; ++e) qf[k][e] = 0.0f;
+      }
     }
-  }
-  float m[GT], l[GT], o[GT][VEC];
 #pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.0f;
+    for (int kp = 0; kp < (GT + 1) / 2; ++kp)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) o[g][e] = 0.0f;
+      for (int e = 0; e < VEC; ++e) q2[kp][e] = pack2(qf[2 * kp][e], 2 * kp + 1 < GT ? qf[2 * kp + 1][e] : 0.0f);
   }
+  float m[GT], l[H];
+  unsigned long long o2[GT][VEC / 2];  // o[k][e], dims packed in pairs
+#pragma unroll
+  for (int k = 0; k < GT; ++k) {
+    m[k] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < VEC / 2; ++e) o2[k][e] = 0ull;
+  }
+#pragma unroll
+  for (int k = 0; k < H; ++k) l[k] = 0.0f;
 
   const int per = (slots + CL - 1) / CL;
   const int lo = min(slots, rank * per), hi = min(slots, lo + per);
@@ -136,14 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (k < nk && nvalid_of(k) == 0) ++k;
     return k;
   };
+  auto issue = [&](int k, int stg) {
+    mbar_arrive_expect_tx(&bars[stg], kTileBytes);
+    bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(slot_of(k)) * 32 * D, kTileBytes, &bars[stg]);
+  };
 
   int ki = next_valid(0), issued = 0;
   while (issued < NST && ki < nk) {
-    if (lane == 0) {
-      const int stg = issued % NST;
-      mbar_arrive_expect_tx(&bars[stg], kTileBytes);
-      bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(slot_of(ki)) * 32 * D, kTileBytes, &bars[stg]);
-    }
+    if (lane == 0) issue(ki, issued % NST);
     ++issued;
     ki = next_valid(ki + 1);
   }
@@ -161,67 +189,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t *kt = reinterpret_cast<const uint16_t *>(ring + stg * kTileBytes);
     const uint16_t *vt = kt + kBlockTokens * D;
 
+    // ---- QK partials: sc[k][i] for head slot k, token u_i = i ^ rot
     float sc[GT][8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int i = 0; i < 8; ++i) {
       float kf[VEC];
-      load_row<VEC>(kt + (2 * u + tsub) * D + dpart * VEC, kf);
+      load_row<VEC>(kt + (2 * (i ^ rot) + tsub) * D + dpart * VEC, kf);
 #pragma unroll
-      for (int g = 0; g < GT; ++g) {
-        float a = 0.0f;
+      for (int kp = 0; kp < (GT + 1) / 2; ++kp) {
+        unsigned long long a = 0ull;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) a = fmaf(qr[g][e], kf[e], a);
-        sc[g][u] = a;
+        for (int e = 0; e < VEC; ++e) a = fma2(q2[kp][e], pack2(kf[e], kf[e]), a);
+        float a0, a1;
+        unpack2(a, a0, a1);
+        sc[2 * kp][i] = a0;
+        if (2 * kp + 1 < GT) sc[2 * kp + 1][i] = a1;
       }
     }
+    // ---- reduce-scatter over the 16 lanes of the half
 #pragma unroll
-    for (int g = 0; g < GT; ++g)
+    for (int k = 0; k < GT; ++k) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float a = sc[g][u];
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 8);
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 4);
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
-        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
-        sc[g][u] = (2 * u + tsub < nv) ? a : -INFINITY;
-      }
+      for (int j = 0; j < 4; ++j) sc[k][j] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][j + 4], 8);
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      float mx = sc[g][0];
-#pragma unroll
-      for (int u = 1; u < 8; ++u) mx = fmaxf(mx, sc[g][u]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-      const float mnew = fmaxf(m[g], mx);
-      const float corr = exp2f(m[g] - mnew);
-      float ps = 0.0f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float p = exp2f(sc[g][u] - mnew);
-        sc[g][u] = p;
-        ps += p;
-      }
-      l[g] = l[g] * corr + ps;
-      m[g] = mnew;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) o[g][e] *= corr;
+      for (int j = 0; j < 2; ++j) sc[k][j] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][j + 2], 4);
+      sc[k][0] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][1], 2);
     }
+    float s_own[H];
+    if constexpr (GT > 1) {
+#pragma unroll
+      for (int k = 0; k < H; ++k) s_own[k] = sc[k][0] + __shfl_xor_sync(0xFFFFFFFFu, sc[k + H][0], 1);
+    } else {
+      s_own[0] = sc[0][0] + __shfl_xor_sync(0xFFFFFFFFu, sc[0][0], 1);
+    }
+    const bool tok_ok = 2 * rot + tsub < nv;
+    // ---- online softmax on the owned logits
+    float mnew[GT];
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+      float v = tok_ok ? s_own[k] : -INFINITY;
+      s_own[k] = v;
+      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 16));
+      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+      mnew[k] = fmaxf(m[k], v);
+    }
+    if constexpr (GT > 1) {
+#pragma unroll
+      for (int k = 0; k < H; ++k) mnew[k + H] = __shfl_xor_sync(0xFFFFFFFFu, mnew[k], 1);
+    }
+    float p_own[H];
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+      p_own[k] = exp2f(s_own[k] - mnew[k]);
+      const float lcorr = exp2f(m[k] - mnew[k]);
+      l[k] = l[k] * lcorr + ((GT > 1 || hb == 0) ? p_own[k] : 0.0f);
+    }
+#pragma unroll
+    for (int k = 0; k < GT; ++k) {
+      const float corr = exp2f(m[k] - mnew[k]);
+      const unsigned long long c2 = pack2(corr, corr);
+#pragma unroll
+      for (int e = 0; e < VEC / 2; ++e) o2[k][e] = fma2(o2[k][e], c2, 0ull);
+      m[k] = mnew[k];
+    }
+    // ---- PV: gather p of this lane's tokens, accumulate its dims
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       float vf[VEC];
       load_row<VEC>(vt + (2 * u + tsub) * D + dpart * VEC, vf);
 #pragma unroll
-      for (int g = 0; g < GT; ++g)
+      for (int k = 0; k < GT; ++k) {
+        const int src = tsub * 16 + 2 * u + (GT > 1 ? ((k >= H) ^ hb) : 0);
+        const float p = __shfl_sync(0xFFFFFFFFu, p_own[GT > 1 ? k % H : 0], src);
+        const unsigned long long p2 = pack2(p, p);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) o[g][e] = fmaf(sc[g][u], vf[e], o[g][e]);
+        for (int e = 0; e < VEC / 2; ++e) o2[k][e] = fma2(p2, pack2(vf[2 * e], vf[2 * e + 1]), o2[k][e]);
+      }
     }
     __syncwarp();
     ++consumed;
     if (ki < nk) {
       if (lane == 0) {
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[stg], kTileBytes);
-        bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(slot_of(ki)) * 32 * D, kTileBytes,
-                 &bars[stg]);
+        issue(ki, stg);
       }
       ++issued;
       ki = next_valid(ki + 1);
@@ -230,28 +282,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (timed_out) {
     if (lane == 0) report(status, OASIS_STATUS_TIMEOUT);
-    for (int c = consumed; c < issued; ++c) mbar_wait_bounded(&bars[c % NST], static_cast<uint32_t>(c / NST) & 1u, kWaitTries);
+    for (int c = consumed; c < issued; ++c)
+      mbar_wait_bounded(&bars[c % NST], static_cast<uint32_t>(c / NST) & 1u, kWaitTries);
   }
 
-  // combine the two token halves of the warp, then the warps of the CTA
+  // ---- per-warp totals: l over the owning lanes, o over the two token halves
 #pragma unroll
-  for (int g = 0; g < GT; ++g) {
-    l[g] += __shfl_xor_sync(0xFFFFFFFFu, l[g], 16);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) o[g][e] += __shfl_xor_sync(0xFFFFFFFFu, o[g][e], 16);
+  for (int k = 0; k < H; ++k) {
+    float v = l[k];
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    if constexpr (GT == 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    l[k] = v;
   }
-  if (lane == 0) {
+  float lfull[GT];
 #pragma unroll
-    for (int g = 0; g < GT; ++g) {
-      wm[warp * GT + g] = m[g];
-      wl[warp * GT + g] = l[g];
+  for (int k = 0; k < H; ++k) lfull[k] = l[k];
+  if constexpr (GT > 1) {
+#pragma unroll
+    for (int k = 0; k < H; ++k) lfull[k + H] = __shfl_xor_sync(0xFFFFFFFFu, l[k], 1);
+  }
+  float of[GT][VEC];
+#pragma unroll
+  for (int k = 0; k < GT; ++k)
+#pragma unroll
+    for (int e = 0; e < VEC / 2; ++e) {
+      float a, b;
+      unpack2(o2[k][e], a, b);
+      of[k][2 * e] = a + __shfl_xor_sync(0xFFFFFFFFu, a, 16);
+      of[k][2 * e + 1] = b + __shfl_xor_sync(0xFFFFFFFFu, b, 16);
+    }
+  __syncthreads();  // every warp is past its ring: the scratch may alias it
+  float *wm = scratch + SM::kWarpM, *wl = scratch + SM::kWarpL, *wo = scratch + SM::kWarpO;
+  float *cm = scratch + SM::kCtaM, *cl = scratch + SM::kCtaL, *co = scratch + SM::kCtaO;
+  if (lane == 0) {  // hb = 0 here: slot k holds head k
+#pragma unroll
+    for (int k = 0; k < GT; ++k) {
+      wm[warp * GT + k] = m[k];
+      wl[warp * GT + k] = lfull[k];
     }
   }
   if (tsub == 0) {
 #pragma unroll
-    for (int g = 0; g < GT; ++g)
+    for (int k = 0; k < GT; ++k) {
+      const int g = GT > 1 ? (k ^ (hb * (GT / 2))) : 0;
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) wo[(warp * GT + g) * D + dpart * VEC + e] = o[g][e];
+      for (int e = 0; e < VEC; ++e) wo[(warp * GT + g) * D + dpart * VEC + e] = of[k][e];
+    }
   }
   __syncthreads();
   for (int idx = tid; idx < GT * D; idx += kThreads) {
@@ -297,30 +376,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster.sync();
 }
 
-int env_int(const char *name, int dflt) {
-  const char *v = std::getenv(name);
-  return v != nullptr ? std::atoi(v) : dflt;
-}
-
 template <int VEC, int GT, int NST>
 cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                      const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
                      int32_t *status, cudaStream_t st) {
-  constexpr int D = 16 * VEC;
+  using SM = Smem<VEC, GT>;
   const int ntiles = (G + GT - 1) / GT;
   const int units = B * Hkv * ntiles;
-  int CL = env_int("OASIS_ATTN_CLUSTER", 0);
-  if (CL <= 0) {
-    CL = 1;
-    while (CL < 8 && units * CL * 2 <= 2 * 152) CL *= 2;
-  }
-  const size_t smem = static_cast<size_t>(kWarps) * NST * 64 * D + sizeof(uint64_t) * kWarps * NST +
-                      sizeof(float) * (2 * kWarps * GT + kWarps * GT * D + 2 * GT + GT * D);
-  cudaError_t e = cudaFuncSetAttribute(k_attn<VEC, GT, NST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t ring = static_cast<size_t>(kWarps) * NST * SM::kTile + sizeof(uint64_t) * kWarps * NST;
+  const size_t smem = std::max(ring, sizeof(float) * SM::kScratchFloats);
+  int sms = 0, per_sm = 0;
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<VEC, GT, NST>), kThreads, smem, &sms,
+                                  &per_sm);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_attn<VEC, GT, NST>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
+  // split every segment over a cluster so that the grid fills the resident CTA slots
+  int CL = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, static_cast<int64_t>(sms) * per_sm / units)));
+  CL = std::min(CL, slots);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(CL), static_cast<unsigned>(units));
   cfg.blockDim = dim3(kThreads);
@@ -342,7 +413,7 @@ template <int VEC>
 cudaError_t launch_vec(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                        const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
                        int32_t *status, cudaStream_t st) {
-  constexpr int NST = VEC == 8 ? 3 : 4;
+  constexpr int NST = 2;
   if (G == 1) return launch_t<VEC, 1, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
   if (G == 2) return launch_t<VEC, 2, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
   if (G <= 4) return launch_t<VEC, 4, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);

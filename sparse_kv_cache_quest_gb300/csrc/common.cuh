@@ -95,6 +95,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 // Launchers implemented by the kernel translation units (host side).
 namespace oasis {
+cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm);
 cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
                                  int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
                                  uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, cudaStream_t st);

@@ -13,16 +13,22 @@
 // other rounds acc + q*sel once, exactly as the sequential definition does.
 // No reassociation, no fast-math: the result is bit-identical to a plain loop.
 //
-// Mapping.  A CTA of 128 threads covers 128*NB consecutive candidate blocks of
-// one segment; thread t owns blocks base + t + 128*i (i < NB).  The chunk-major
-// summary layout [S][D/8][Nb][8] makes every 16-byte load of a warp part of
-// one contiguous 512-byte run.  Accumulators of block pairs are packed fp32x2
-// registers (fma.rn.f32x2), which halves the issue slots of the FMAs; the
-// query operands sit in shared memory pre-split and pre-duplicated as
-// {qp, qp, qn, qn}, one broadcast 16-byte load per (query, dim) feeding 2*NB/2
-// packed FMAs.  Queries are processed in tiles of QT (padded by repeating the
-// last query, which leaves the max unchanged); the next 8-dim chunk is loaded
-// while the current one is consumed.
+// Work split.  The unit of work is 32 consecutive candidate blocks of one
+// segment, one block per lane of a warp.  Units are numbered segment-major and
+// each CTA of a persistent grid (SM count x resident CTAs per SM) takes one
+// contiguous range of units, so every SM gets the same number of units (+-1)
+// whatever the segment count.  A CTA walks the segments of its range in phases
+// of at most `qseg` segments whose query operands it holds in shared memory;
+// its warps take the units of a phase round-robin.
+//
+// Inner loop.  Lane b streams its block's 16-byte kmin/kmax chunks (8 dims of
+// the chunk-major layout [S][D/8][Nb][8], so a warp reads 512 contiguous bytes
+// per load) with kPF chunks in flight.  Per dim it widens kmin/kmax to fp32 and
+// runs two packed fp32x2 FMAs (fma.rn.f32x2) per pair of queries: the query
+// operands sit in shared memory as {qn_j, qn_j+1, qp_j, qp_j+1}, one broadcast
+// 16-byte load per pair and dim.  Queries are padded to NQP by repeating the
+// last one, which leaves the max unchanged.
+#include <algorithm>
 #include <cfloat>
 
 #include "common.cuh"
@@ -30,147 +36,144 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnit = 32;  // blocks per unit (one per lane)
 
-template <int NB, int QT>
-__global__ void __launch_bounds__(kThreads) k_score(const uint16_t *__restrict__ kmin,
-                                                    const uint16_t *__restrict__ kmax, int Nb_max,
-                                                    const uint16_t *__restrict__ qdraft, int Hkv, int G, int Nd,
-                                                    int D, const int32_t *__restrict__ seq_len, int W,
-                                                    float *__restrict__ scores, int32_t *status) {
-  static_assert(NB % 2 == 0, "blocks are processed in packed pairs");
-  extern __shared__ float4 qsm[];  // [D][nqp] {qp, qp, qn, qn}
-  const int s = blockIdx.y;
-  const int bseq = s / Hkv, h = s % Hkv;
-  const int Nq = G * Nd;
-  const int nqp = ((Nq + QT - 1) / QT) * QT;
-  const int L = load_len(seq_len, bseq, Nb_max * kBlockTokens, status,
-                         blockIdx.x == 0 && threadIdx.x == 0 && h == 0);
-  const int nc = ceil_div(L, kBlockTokens) - W;
-  const int base = blockIdx.x * kThreads * NB;
-  if (base >= nc) return;  // uniform across the CTA
+// Two CTAs per SM (<= 64 registers per thread) while the accumulators allow it.
+template <int NQP>
+constexpr int min_ctas() { return NQP <= 12 ? 2 : 1; }
+template <int NQP>
+constexpr size_t smem_budget() { return NQP <= 12 ? 100 * 1024 : 200 * 1024; }
+// chunks in flight per lane
+template <int NQP>
+constexpr int prefetch() { return NQP <= 12 ? 2 : 3; }
 
-  const int Hq = Hkv * G;
-  for (int idx = threadIdx.x; idx < D * nqp; idx += kThreads) {
-    const int d = idx / nqp;
-    const int j = min(idx % nqp, Nq - 1);
-    const int jd = j / G, g = j % G;
-    const uint16_t raw = qdraft[((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + d];
-    const float q = __uint_as_float(static_cast<uint32_t>(raw) << 16);
-    const bool pos = q >= 0.0f;
-    const float qp = pos ? q : 0.0f, qn = pos ? 0.0f : q;
-    qsm[idx] = make_float4(qp, qp, qn, qn);
-  }
-  __syncthreads();
+// CH = D / 8 chunks of 8 dims (8 for D = 64, 16 for D = 128).
+template <int NQP, int CH>
+__global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
+    k_score(const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax, int Nb_max,
+            const uint16_t *__restrict__ qdraft, int S, int Hkv, int G, int Nd, const int32_t *__restrict__ seq_len,
+            int W, float *__restrict__ scores, int32_t *status, int units_per_seg, int qseg) {
+  constexpr int D = CH * 8;
+  constexpr int per_seg_q = D * (NQP / 2);
+  constexpr int kPF = prefetch<NQP>();
+  extern __shared__ float4 qsm[];  // [qseg][D][NQP/2] {qn_j, qn_j+1, qp_j, qp_j+1}
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t U = static_cast<int64_t>(S) * units_per_seg;
+  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  if (u0 >= u1) return;
+  const int Nq = G * Nd, Hq = Hkv * G;
+  const int s_last = static_cast<int>((u1 - 1) / units_per_seg);
 
-  int blk[NB];
+  for (int s_lo = static_cast<int>(u0 / units_per_seg); s_lo <= s_last; s_lo += qseg) {
+    const int s_hi = min(s_last + 1, s_lo + qseg);  // segments [s_lo, s_hi) in this phase
+    __syncthreads();                                // the previous phase is done with qsm
+    for (int idx = tid; idx < (s_hi - s_lo) * per_seg_q; idx += kThreads) {
+      const int sl = idx / per_seg_q, rem = idx % per_seg_q;
+      const int d = rem / (NQP / 2), jp = rem % (NQP / 2);
+      const int s = s_lo + sl, bseq = s / Hkv, h = s % Hkv;
+      float qv[2];
 #pragma unroll
-  for (int i = 0; i < NB; ++i) blk[i] = min(base + static_cast<int>(threadIdx.x) + kThreads * i, nc - 1);
-  const int chunks = D >> 3;
-  const uint4 *pmin = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * chunks * Nb_max;
-  const uint4 *pmax = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * chunks * Nb_max;
-
-  float best[NB];
-#pragma unroll
-  for (int i = 0; i < NB; ++i) best[i] = -FLT_MAX;
-  bool first_tile = true;
-
-  for (int q0 = 0; q0 < nqp; q0 += QT) {
-    unsigned long long acc[NB / 2][QT];
-#pragma unroll
-    for (int p = 0; p < NB / 2; ++p)
-#pragma unroll
-      for (int jj = 0; jj < QT; ++jj) acc[p][jj] = 0ull;  // (+0, +0)
-
-    uint4 cmn[NB], cmx[NB];
-#pragma unroll
-    for (int i = 0; i < NB; ++i) {
-      cmn[i] = __ldg(pmin + blk[i]);
-      cmx[i] = __ldg(pmax + blk[i]);
-    }
-    for (int c = 0; c < chunks; ++c) {
-      uint4 nmn[NB], nmx[NB];
-      const int cn = c + 1 < chunks ? c + 1 : c;
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        nmn[i] = __ldg(pmin + static_cast<int64_t>(cn) * Nb_max + blk[i]);
-        nmx[i] = __ldg(pmax + static_cast<int64_t>(cn) * Nb_max + blk[i]);
+      for (int t = 0; t < 2; ++t) {
+        const int j = min(2 * jp + t, Nq - 1);
+        const int jd = j / G, g = j % G;
+        const uint16_t raw = qdraft[((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + d];
+        qv[t] = __uint_as_float(static_cast<uint32_t>(raw) << 16);
       }
-      const float4 *qrow = qsm + (c * 8) * nqp + q0;
+      const bool p0 = qv[0] >= 0.0f, p1 = qv[1] >= 0.0f;
+      qsm[idx] = make_float4(p0 ? 0.0f : qv[0], p1 ? 0.0f : qv[1], p0 ? qv[0] : 0.0f, p1 ? qv[1] : 0.0f);
+    }
+    __syncthreads();
+
+    const int64_t pu0 = std::max(u0, static_cast<int64_t>(s_lo) * units_per_seg);
+    const int64_t pu1 = std::min(u1, static_cast<int64_t>(s_hi) * units_per_seg);
+    for (int64_t u = pu0 + warp; u < pu1; u += kWarps) {
+      const int s = static_cast<int>(u / units_per_seg);
+      const int base = static_cast<int>(u % units_per_seg) * kUnit;
+      const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status,
+                             lane == 0 && base == 0 && (s % Hkv) == 0);
+      const int nc = ceil_div(L, kBlockTokens) - W;
+      if (base >= nc) continue;  // warp-uniform
+      const int b = base + lane;
+      const int bl = min(b, nc - 1);
+      const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max + bl;
+      const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max + bl;
+      const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
+
+      unsigned long long acc[NQP / 2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        unsigned long long kn2[NB / 2], kx2[NB / 2];
+      for (int jp = 0; jp < NQP / 2; ++jp) acc[jp] = 0ull;  // (+0, +0)
+      uint4 bmn[kPF], bmx[kPF];
 #pragma unroll
-        for (int p = 0; p < NB / 2; ++p) {
-          const uint32_t wn0 = (&cmn[2 * p].x)[e >> 1], wn1 = (&cmn[2 * p + 1].x)[e >> 1];
-          const uint32_t wx0 = (&cmx[2 * p].x)[e >> 1], wx1 = (&cmx[2 * p + 1].x)[e >> 1];
-          if (e & 1) {
-            kn2[p] = pack2(bf16_hi(wn0), bf16_hi(wn1));
-            kx2[p] = pack2(bf16_hi(wx0), bf16_hi(wx1));
-          } else {
-            kn2[p] = pack2(bf16_lo(wn0), bf16_lo(wn1));
-            kx2[p] = pack2(bf16_lo(wx0), bf16_lo(wx1));
+      for (int p = 0; p < kPF; ++p) {
+        bmn[p] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max);
+        bmx[p] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max);
+      }
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const uint4 mn = bmn[c % kPF], mx = bmx[c % kPF];
+        if (c + kPF < CH) {
+          bmn[c % kPF] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max);
+          bmx[c % kPF] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max);
+        }
+        const float4 *qrow = qbase + (c * 8) * (NQP / 2);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t wn = e < 2 ? mn.x : e < 4 ? mn.y : e < 6 ? mn.z : mn.w;
+          const uint32_t wx = e < 2 ? mx.x : e < 4 ? mx.y : e < 6 ? mx.z : mx.w;
+          const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
+          const float fx = (e & 1) ? bf16_hi(wx) : bf16_lo(wx);
+          const unsigned long long kn2 = pack2(fn, fn), kx2 = pack2(fx, fx);
+#pragma unroll
+          for (int jp = 0; jp < NQP / 2; ++jp) {
+            const float4 qv = qrow[e * (NQP / 2) + jp];
+            acc[jp] = fma2(pack2(qv.x, qv.y), kn2, acc[jp]);
+            acc[jp] = fma2(pack2(qv.z, qv.w), kx2, acc[jp]);
           }
         }
-#pragma unroll
-        for (int jj = 0; jj < QT; ++jj) {
-          const float4 qv = qrow[e * nqp + jj];
-          const unsigned long long qp2 = pack2(qv.x, qv.y), qn2 = pack2(qv.z, qv.w);
-#pragma unroll
-          for (int p = 0; p < NB / 2; ++p) {
-            acc[p][jj] = fma2(qn2, kn2[p], acc[p][jj]);
-            acc[p][jj] = fma2(qp2, kx2[p], acc[p][jj]);
-          }
-        }
       }
+      float best = -FLT_MAX;
 #pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        cmn[i] = nmn[i];
-        cmx[i] = nmx[i];
-      }
-    }
-#pragma unroll
-    for (int p = 0; p < NB / 2; ++p)
-#pragma unroll
-      for (int jj = 0; jj < QT; ++jj) {
+      for (int jp = 0; jp < NQP / 2; ++jp) {
         float a0, a1;
-        unpack2(acc[p][jj], a0, a1);
-        if (first_tile && jj == 0) {
-          best[2 * p] = a0;
-          best[2 * p + 1] = a1;
-        } else {
-          best[2 * p] = fmaxf(best[2 * p], a0);
-          best[2 * p + 1] = fmaxf(best[2 * p + 1], a1);
-        }
+        unpack2(acc[jp], a0, a1);
+        best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
       }
-    first_tile = false;
-  }
-
-  float *out = scores + static_cast<int64_t>(s) * Nb_max;
-#pragma unroll
-  for (int i = 0; i < NB; ++i) {
-    const int b = base + static_cast<int>(threadIdx.x) + kThreads * i;
-    if (b < nc) out[b] = best[i];
+      if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
+    }
   }
 }
 
-template <int NB, int QT>
-cudaError_t launch_nb_qt(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
-                         int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W, float *scores,
-                         int32_t *status, cudaStream_t st) {
-  const int Nq = G * Nd;
-  const int nqp = ((Nq + QT - 1) / QT) * QT;
-  const size_t smem = sizeof(float4) * static_cast<size_t>(D) * nqp;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_score<NB, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  const dim3 grid(static_cast<unsigned>((Nb_max + kThreads * NB - 1) / (kThreads * NB)),
-                  static_cast<unsigned>(B * Hkv));
-  k_score<NB, QT><<<grid, kThreads, smem, st>>>(kmin, kmax, Nb_max, qdraft, Hkv, G, Nd, D, seq_len, W, scores,
-                                                 status);
+template <int NQP, int CH>
+cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
+                          int Hkv, int G, int Nd, const int32_t *seq_len, int W, float *scores, int32_t *status,
+                          cudaStream_t st) {
+  constexpr int D = CH * 8;
+  const int S = B * Hkv;
+  const int ncand = std::max(1, Nb_max - W);
+  const int units_per_seg = (ncand + kUnit - 1) / kUnit;
+  const int64_t U = static_cast<int64_t>(S) * units_per_seg;
+  const size_t per_seg = sizeof(float4) * static_cast<size_t>(D) * (NQP / 2);
+  const int qseg = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, smem_budget<NQP>() / per_seg)));
+  const size_t smem = per_seg * qseg;
+  int sms = 0, per_sm = 0;
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score<NQP, CH>), kThreads, smem, &sms, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t want = static_cast<int64_t>(sms) * per_sm;
+  const int grid = static_cast<int>(std::min<int64_t>(want, std::max<int64_t>(1, (U + kWarps - 1) / kWarps)));
+  k_score<NQP, CH><<<grid, kThreads, smem, st>>>(kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W, scores,
+                                                  status, units_per_seg, qseg);
   return cudaGetLastError();
+}
+
+template <int NQP>
+cudaError_t launch_nqp(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
+                       int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W, float *scores,
+                       int32_t *status, cudaStream_t st) {
+  if (D == 128)
+    return launch_nqp_ch<NQP, 16>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, status, st);
+  return launch_nqp_ch<NQP, 8>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, status, st);
 }
 
 }  // namespace
@@ -179,11 +182,19 @@ cudaError_t launch_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int 
                                 int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
                                 float *scores, int32_t *status, cudaStream_t st) {
   const int Nq = G * Nd;
-  if (Nq <= 2) return launch_nb_qt<4, 2>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
-  if (Nq <= 4) return launch_nb_qt<4, 4>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
-  if (Nq <= 8) return launch_nb_qt<4, 8>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
-  if (Nq <= 12) return launch_nb_qt<4, 12>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
-  return launch_nb_qt<4, 16>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
+#define OASIS_SCORE_CASE(N) \
+  if (Nq <= N) return launch_nqp<N>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status, st);
+  OASIS_SCORE_CASE(2)
+  OASIS_SCORE_CASE(4)
+  OASIS_SCORE_CASE(8)
+  OASIS_SCORE_CASE(12)
+  OASIS_SCORE_CASE(16)
+  OASIS_SCORE_CASE(24)
+  OASIS_SCORE_CASE(32)
+  OASIS_SCORE_CASE(48)
+  OASIS_SCORE_CASE(64)
+#undef OASIS_SCORE_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace oasis
