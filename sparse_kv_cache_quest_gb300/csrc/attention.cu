@@ -9,8 +9,9 @@
 //
 // Data path.  A segment's pool is slots_per_seg contiguous 8 KiB tiles (K then
 // V, D = 128).  The segment is split over a thread-block cluster of CL CTAs
-// (split-K): CTA rank r takes a contiguous slot range, and inside it warp w
-// takes every 4th slot.  Each warp streams its tiles through a private ring of
+// (split-K): the CL*4 warps of the cluster take the slots round-robin.  Each
+// warp first lists its non-empty slots in shared memory (one table read per
+// slot, off the streaming loop), then streams their tiles through a ring of
 // NST shared-memory stages with 1-D bulk async copies (cp.async.bulk, one
 // mbarrier per stage, lane 0 issues), so the next tile is in flight while one
 // is consumed.  Empty slots and slots without valid tokens are never loaded.
@@ -79,7 +80,7 @@ template <int VEC, int GT, int NST>
 __global__ void __launch_bounds__(kThreads)
     k_attn(const uint16_t *__restrict__ q, const uint16_t *__restrict__ pool, const int32_t *__restrict__ table,
            int slots, const int32_t *__restrict__ seq_len, int Hkv, int G, int ntiles, float scale_log2,
-           float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
+           float *__restrict__ out, float *__restrict__ lse, int32_t *status, int list_cap) {
   using SM = Smem<VEC, GT>;
   constexpr int D = SM::D;
   constexpr uint32_t kTileBytes = SM::kTile;
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(kThreads)
   unsigned char *ring = sm + static_cast<size_t>(warp) * NST * kTileBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + static_cast<size_t>(kWarps) * NST * kTileBytes) + warp * NST;
   float *scratch = reinterpret_cast<float *>(sm);  // used only once every ring stage is drained
+  int32_t *list = reinterpret_cast<int32_t *>(bars + (kWarps - warp) * NST) + warp * list_cap;
 
   if (lane == 0) {
     for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
@@ -148,44 +150,44 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int k = 0; k < H; ++k) l[k] = 0.0f;
 
-  const int per = (slots + CL - 1) / CL;
-  const int lo = min(slots, rank * per), hi = min(slots, lo + per);
-  const int nk = hi - lo > warp ? (hi - lo - warp + kWarps - 1) / kWarps : 0;
+  // this warp's slots: gw, gw + nw, ... over the whole cluster; the non-empty ones
+  // (slot << 5 | valid tokens) go to a per-warp list in shared memory, so the
+  // streaming loop below makes no global-memory round trip for control flow
+  const int nw = CL * kWarps, gw = rank * kWarps + warp;
+  const int nk = slots > gw ? (slots - gw + nw - 1) / nw : 0;
   const int32_t *trow = table + static_cast<int64_t>(s) * slots;
   const uint16_t *prow = pool + static_cast<int64_t>(s) * slots * 32 * D;
-  auto slot_of = [&](int k) { return lo + warp + kWarps * k; };
-  auto nvalid_of = [&](int k) {
-    const int blk = trow[slot_of(k)];
-    if (blk < 0) return 0;
-    const int64_t n = static_cast<int64_t>(L) - static_cast<int64_t>(kBlockTokens) * blk;
-    return n <= 0 ? 0 : (n >= kBlockTokens ? kBlockTokens : static_cast<int>(n));
-  };
-  auto next_valid = [&](int k) {
-    while (k < nk && nvalid_of(k) == 0) ++k;
-    return k;
-  };
-  auto issue = [&](int k, int stg) {
-    mbar_arrive_expect_tx(&bars[stg], kTileBytes);
-    bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(slot_of(k)) * 32 * D, kTileBytes, &bars[stg]);
-  };
-
-  int ki = next_valid(0), issued = 0;
-  while (issued < NST && ki < nk) {
-    if (lane == 0) issue(ki, issued % NST);
-    ++issued;
-    ki = next_valid(ki + 1);
+  int count = 0;
+  for (int base = 0; base < nk; base += 32) {
+    const int k = base + lane;
+    int nv = 0, slot = 0;
+    if (k < nk) {
+      slot = gw + nw * k;
+      const int blk = trow[slot];
+      const int64_t n = blk < 0 ? 0 : static_cast<int64_t>(L) - static_cast<int64_t>(kBlockTokens) * blk;
+      nv = n <= 0 ? 0 : (n >= kBlockTokens ? kBlockTokens : static_cast<int>(n));
+    }
+    const unsigned mk = __ballot_sync(0xFFFFFFFFu, nv > 0);
+    if (nv > 0) list[count + __popc(mk & ((1u << lane) - 1u))] = (slot << 5) | nv;
+    count += __popc(mk);
   }
-
-  int kc = next_valid(0), consumed = 0;
+  __syncwarp();
+  auto issue = [&](int c, int stg) {
+    mbar_arrive_expect_tx(&bars[stg], kTileBytes);
+    bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(list[c] >> 5) * 32 * D, kTileBytes, &bars[stg]);
+  };
+  if (lane == 0)
+    for (int c = 0; c < NST && c < count; ++c) issue(c, c);
+  int issued = min(NST, count), consumed = 0;
   bool timed_out = false;
-  while (kc < nk) {
-    const int stg = consumed % NST;
-    const bool ok = mbar_wait_bounded(&bars[stg], static_cast<uint32_t>(consumed / NST) & 1u, kWaitTries);
+  for (int c = 0; c < count; ++c) {
+    const int stg = c % NST;
+    const bool ok = mbar_wait_bounded(&bars[stg], static_cast<uint32_t>(c / NST) & 1u, kWaitTries);
     if (__any_sync(0xFFFFFFFFu, !ok)) {
       timed_out = true;
       break;
     }
-    const int nv = nvalid_of(kc);
+    const int nv = list[c] & 31;
     const uint16_t *kt = reinterpret_cast<const uint16_t *>(ring + stg * kTileBytes);
     const uint16_t *vt = kt + kBlockTokens * D;
 
@@ -270,15 +272,13 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncwarp();
     ++consumed;
-    if (ki < nk) {
+    if (c + NST < count) {
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue(ki, stg);
+        issue(c + NST, stg);
       }
       ++issued;
-      ki = next_valid(ki + 1);
     }
-    kc = next_valid(kc + 1);
   }
   if (timed_out) {
     if (lane == 0) report(status, OASIS_STATUS_TIMEOUT);
@@ -384,7 +384,10 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   const int ntiles = (G + GT - 1) / GT;
   const int units = B * Hkv * ntiles;
   const size_t ring = static_cast<size_t>(kWarps) * NST * SM::kTile + sizeof(uint64_t) * kWarps * NST;
-  const size_t smem = std::max(ring, sizeof(float) * SM::kScratchFloats);
+  // the shared-memory size (and so the occupancy) is fixed by the rings; the slot
+  // lists take a fixed maximum of kListMax entries per warp
+  constexpr int kListMax = 512;
+  const size_t smem = std::max(ring + sizeof(int32_t) * kWarps * kListMax, sizeof(float) * SM::kScratchFloats);
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<VEC, GT, NST>), kThreads, smem, &sms,
                                   &per_sm);
@@ -392,6 +395,9 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   // split every segment over a cluster so that the grid fills the resident CTA slots
   int CL = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, static_cast<int64_t>(sms) * per_sm / units)));
   CL = std::min(CL, slots);
+  while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // keep each warp's list within kListMax
+  if (CL > 8) return cudaErrorInvalidValue;
+  const int list_cap = kListMax;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(CL), static_cast<unsigned>(units));
   cfg.blockDim = dim3(kThreads);
@@ -406,7 +412,7 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   cfg.numAttrs = 1;
   const float scale_log2 = scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&cfg, k_attn<VEC, GT, NST>, q, pool, table, slots, seq_len, Hkv, G, ntiles,
-                            scale_log2, out, lse, status);
+                            scale_log2, out, lse, status, list_cap);
 }
 
 template <int VEC>

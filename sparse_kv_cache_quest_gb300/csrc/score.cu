@@ -13,8 +13,8 @@
 // other rounds acc + q*sel once, exactly as the sequential definition does.
 // No reassociation, no fast-math: the result is bit-identical to a plain loop.
 //
-// Work split.  The unit of work is 32 consecutive candidate blocks of one
-// segment, one block per lane of a warp.  Units are numbered segment-major and
+// Work split.  The unit of work is 32*NB consecutive candidate blocks of one
+// segment, NB blocks per lane of a warp (NB = 2 while the accumulators fit).  Units are numbered segment-major and
 // each CTA of a persistent grid (SM count x resident CTAs per SM) takes one
 // contiguous range of units, so every SM gets the same number of units (+-1)
 // whatever the segment count.  A CTA walks the segments of its range in phases
@@ -24,9 +24,9 @@
 // Inner loop.  Lane b streams its block's 16-byte kmin/kmax chunks (8 dims of
 // the chunk-major layout [S][D/8][Nb][8], so a warp reads 512 contiguous bytes
 // per load) with kPF chunks in flight.  Per dim it widens kmin/kmax to fp32 and
-// runs two packed fp32x2 FMAs (fma.rn.f32x2) per pair of queries: the query
-// operands sit in shared memory as {qn_j, qn_j+1, qp_j, qp_j+1}, one broadcast
-// 16-byte load per pair and dim.  Queries are padded to NQP by repeating the
+// runs two packed fp32x2 FMAs (fma.rn.f32x2) per pair of queries and block:
+// the query operands sit in shared memory as {qn_j, qn_j+1, qp_j, qp_j+1}, one
+// broadcast 16-byte load per pair and dim feeding 2*NB packed FMAs.  Queries are padded to NQP by repeating the
 // last one, which leaves the max unchanged.
 #include <algorithm>
 #include <cfloat>
@@ -36,18 +36,19 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnit = 32;  // blocks per unit (one per lane)
 
-// Two CTAs per SM (<= 64 registers per thread) while the accumulators allow it.
+// Blocks per lane: two while the accumulators fit (each broadcast query load
+// then feeds four packed FMAs instead of two), else one.
 template <int NQP>
-constexpr int min_ctas() { return NQP <= 12 ? 2 : 1; }
+constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
 template <int NQP>
-constexpr size_t smem_budget() { return NQP <= 12 ? 100 * 1024 : 200 * 1024; }
-// chunks in flight per lane
+constexpr int min_ctas() { return 2; }
 template <int NQP>
-constexpr int prefetch() { return NQP <= 12 ? 2 : 3; }
+constexpr size_t smem_budget() { return 100 * 1024; }
+template <int NQP>
+constexpr int prefetch() { return 2; }  // chunks in flight per lane and block
 
 // CH = D / 8 chunks of 8 dims (8 for D = 64, 16 for D = 128).
 template <int NQP, int CH>
@@ -58,6 +59,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
   constexpr int D = CH * 8;
   constexpr int per_seg_q = D * (NQP / 2);
   constexpr int kPF = prefetch<NQP>();
+  constexpr int NB = blocks_per_lane<NQP>();
+  constexpr int kUnit = 32 * NB;  // blocks per warp unit
   extern __shared__ float4 qsm[];  // [qseg][D][NQP/2] {qn_j, qn_j+1, qp_j, qp_j+1}
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
@@ -95,52 +98,75 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
                              lane == 0 && base == 0 && (s % Hkv) == 0);
       const int nc = ceil_div(L, kBlockTokens) - W;
       if (base >= nc) continue;  // warp-uniform
-      const int b = base + lane;
-      const int bl = min(b, nc - 1);
-      const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max + bl;
-      const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max + bl;
+      int bl[NB];
+#pragma unroll
+      for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, nc - 1);
+      const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
+      const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
       const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
 
-      unsigned long long acc[NQP / 2];
+      unsigned long long acc[NB][NQP / 2];
 #pragma unroll
-      for (int jp = 0; jp < NQP / 2; ++jp) acc[jp] = 0ull;  // (+0, +0)
-      uint4 bmn[kPF], bmx[kPF];
+      for (int i = 0; i < NB; ++i)
 #pragma unroll
-      for (int p = 0; p < kPF; ++p) {
-        bmn[p] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max);
-        bmx[p] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max);
-      }
+        for (int jp = 0; jp < NQP / 2; ++jp) acc[i][jp] = 0ull;  // (+0, +0)
+      uint4 bmn[kPF][NB], bmx[kPF][NB];
+#pragma unroll
+      for (int p = 0; p < kPF; ++p)
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
+          bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
+        }
 #pragma unroll
       for (int c = 0; c < CH; ++c) {
-        const uint4 mn = bmn[c % kPF], mx = bmx[c % kPF];
-        if (c + kPF < CH) {
-          bmn[c % kPF] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max);
-          bmx[c % kPF] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max);
+        uint4 mn[NB], mx[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          mn[i] = bmn[c % kPF][i];
+          mx[i] = bmx[c % kPF][i];
+          if (c + kPF < CH) {
+            bmn[c % kPF][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+            bmx[c % kPF][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+          }
         }
         const float4 *qrow = qbase + (c * 8) * (NQP / 2);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint32_t wn = e < 2 ? mn.x : e < 4 ? mn.y : e < 6 ? mn.z : mn.w;
-          const uint32_t wx = e < 2 ? mx.x : e < 4 ? mx.y : e < 6 ? mx.z : mx.w;
-          const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
-          const float fx = (e & 1) ? bf16_hi(wx) : bf16_lo(wx);
-          const unsigned long long kn2 = pack2(fn, fn), kx2 = pack2(fx, fx);
+          unsigned long long kn2[NB], kx2[NB];
+#pragma unroll
+          for (int i = 0; i < NB; ++i) {
+            const uint32_t wn = e < 2 ? mn[i].x : e < 4 ? mn[i].y : e < 6 ? mn[i].z : mn[i].w;
+            const uint32_t wx = e < 2 ? mx[i].x : e < 4 ? mx[i].y : e < 6 ? mx[i].z : mx[i].w;
+            const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
+            const float fx = (e & 1) ? bf16_hi(wx) : bf16_lo(wx);
+            kn2[i] = pack2(fn, fn);
+            kx2[i] = pack2(fx, fx);
+          }
 #pragma unroll
           for (int jp = 0; jp < NQP / 2; ++jp) {
             const float4 qv = qrow[e * (NQP / 2) + jp];
-            acc[jp] = fma2(pack2(qv.x, qv.y), kn2, acc[jp]);
-            acc[jp] = fma2(pack2(qv.z, qv.w), kx2, acc[jp]);
+            const unsigned long long qn2 = pack2(qv.x, qv.y), qp2 = pack2(qv.z, qv.w);
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+              acc[i][jp] = fma2(qn2, kn2[i], acc[i][jp]);
+              acc[i][jp] = fma2(qp2, kx2[i], acc[i][jp]);
+            }
           }
         }
       }
-      float best = -FLT_MAX;
 #pragma unroll
-      for (int jp = 0; jp < NQP / 2; ++jp) {
-        float a0, a1;
-        unpack2(acc[jp], a0, a1);
-        best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
+      for (int i = 0; i < NB; ++i) {
+        float best = -FLT_MAX;
+#pragma unroll
+        for (int jp = 0; jp < NQP / 2; ++jp) {
+          float a0, a1;
+          unpack2(acc[i][jp], a0, a1);
+          best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
+        }
+        const int b = base + lane + 32 * i;
+        if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
       }
-      if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
     }
   }
 }
@@ -152,6 +178,7 @@ cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max
   constexpr int D = CH * 8;
   const int S = B * Hkv;
   const int ncand = std::max(1, Nb_max - W);
+  constexpr int kUnit = 32 * blocks_per_lane<NQP>();
   const int units_per_seg = (ncand + kUnit - 1) / kUnit;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
   const size_t per_seg = sizeof(float4) * static_cast<size_t>(D) * (NQP / 2);
@@ -161,7 +188,7 @@ cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score<NQP, CH>), kThreads, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
-  const int grid = static_cast<int>(std::min<int64_t>(want, std::max<int64_t>(1, (U + kWarps - 1) / kWarps)));
+  const int grid = static_cast<int>(std::min<int64_t>(want, U));  // every CTA gets >= 1 unit
   k_score<NQP, CH><<<grid, kThreads, smem, st>>>(kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W, scores,
                                                   status, units_per_seg, qseg);
   return cudaGetLastError();

@@ -4,10 +4,11 @@
 // every logical block keeps a per-dimension min/max of its keys, 1/16 of the
 // full KV; §5: compressed keys are updated during decode.
 //
-// One thread per (segment, block, 8-dim chunk): it reads the chunk's 16 bytes
-// from each valid token row (consecutive threads read consecutive chunks of a
-// row, so a warp reads whole 256-byte rows) and writes 16 bytes to kmin and
-// kmax in the chunk-major layout [S][D/8][Nb_max][8].
+// One thread per (segment, block, 8-dim chunk), over a flat grid: it issues
+// the 16-byte loads of the chunk from all valid token rows at once
+// (consecutive threads read consecutive chunks of a row, so a warp reads whole
+// 256-byte rows) and writes 16 bytes to kmin and kmax in the chunk-major
+// layout [S][D/8][Nb_max][8].
 //
 // min/max use the IEEE 754-2019 total order of non-NaN values (-0 below +0):
 // each bf16 bit pattern u maps to the 16-bit key u | 0x8000 (u >= +0) or ~u
@@ -31,36 +32,41 @@ __device__ __forceinline__ uint32_t from_key2(uint32_t k) {
 __global__ void __launch_bounds__(256) k_build_summary(const uint16_t *__restrict__ k, int64_t seg_stride,
                                                        int64_t blk_stride, int64_t tok_stride, int Hkv, int D,
                                                        const int32_t *__restrict__ seq_len, int blk_begin,
-                                                       int blk_count, uint16_t *__restrict__ kmin,
+                                                       int blk_count, int S, uint16_t *__restrict__ kmin,
                                                        uint16_t *__restrict__ kmax, int Nb_max,
                                                        int32_t *status) {
-  const int s = blockIdx.y;
   const int chunks = D >> 3;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status,
-                         blockIdx.x == 0 && threadIdx.x == 0 && (s % Hkv) == 0);
-  if (item >= static_cast<int64_t>(blk_count) * chunks) return;
-  const int j = static_cast<int>(item / chunks);
+  if (item >= static_cast<int64_t>(S) * blk_count * chunks) return;
   const int c = static_cast<int>(item % chunks);
+  const int64_t sj = item / chunks;
+  const int j = static_cast<int>(sj % blk_count);
+  const int s = static_cast<int>(sj / blk_count);
+  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status, j == 0 && c == 0 && (s % Hkv) == 0);
   const int b = blk_begin + j;
   const int nvalid = min(kBlockTokens, L - kBlockTokens * b);
   if (nvalid <= 0) return;
 
   const uint16_t *p = k + s * seg_stride + j * blk_stride + c * 8;
+  uint4 v[kBlockTokens];
+#pragma unroll
+  for (int t = 0; t < kBlockTokens; ++t)  // all loads in flight at once
+    if (t < nvalid) v[t] = __ldg(reinterpret_cast<const uint4 *>(p + t * tok_stride));
   uint4 lo = make_uint4(0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu);
   uint4 hi = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 4
-  for (int t = 0; t < nvalid; ++t) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p + t * tok_stride));
-    const uint32_t a = to_key2(v.x), bb = to_key2(v.y), cc = to_key2(v.z), dd = to_key2(v.w);
-    lo.x = __vminu2(lo.x, a);
-    lo.y = __vminu2(lo.y, bb);
-    lo.z = __vminu2(lo.z, cc);
-    lo.w = __vminu2(lo.w, dd);
-    hi.x = __vmaxu2(hi.x, a);
-    hi.y = __vmaxu2(hi.y, bb);
-    hi.z = __vmaxu2(hi.z, cc);
-    hi.w = __vmaxu2(hi.w, dd);
+#pragma unroll
+  for (int t = 0; t < kBlockTokens; ++t) {
+    if (t < nvalid) {
+      const uint32_t a = to_key2(v[t].x), bb = to_key2(v[t].y), cc = to_key2(v[t].z), dd = to_key2(v[t].w);
+      lo.x = __vminu2(lo.x, a);
+      lo.y = __vminu2(lo.y, bb);
+      lo.z = __vminu2(lo.z, cc);
+      lo.w = __vminu2(lo.w, dd);
+      hi.x = __vmaxu2(hi.x, a);
+      hi.y = __vmaxu2(hi.y, bb);
+      hi.z = __vmaxu2(hi.z, cc);
+      hi.w = __vmaxu2(hi.w, dd);
+    }
   }
   const int64_t o = ((static_cast<int64_t>(s) * chunks + c) * Nb_max + b) * 8;
   *reinterpret_cast<uint4 *>(kmin + o) =
@@ -75,11 +81,13 @@ cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t 
                                  int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
                                  uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, cudaStream_t st) {
   const int S = B * Hkv;
-  const int64_t items = static_cast<int64_t>(blk_count) * (D / 8);
+  const int64_t items = static_cast<int64_t>(S) * blk_count * (D / 8);
   const int threads = 256;
-  const dim3 grid(static_cast<unsigned>((items + threads - 1) / threads), static_cast<unsigned>(S));
-  k_build_summary<<<grid, threads, 0, st>>>(k, seg_stride, blk_stride, tok_stride, Hkv, D, seq_len, blk_begin,
-                                            blk_count, kmin, kmax, Nb_max, status);
+  const int64_t grid = (items + threads - 1) / threads;
+  if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  k_build_summary<<<static_cast<unsigned>(grid), threads, 0, st>>>(k, seg_stride, blk_stride, tok_stride, Hkv, D,
+                                                                  seq_len, blk_begin, blk_count, S, kmin, kmax,
+                                                                  Nb_max, status);
   return cudaGetLastError();
 }
 
