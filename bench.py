@@ -40,10 +40,11 @@ WORKLOAD_ID = 2
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=8000)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=14400, help="layer-steps timed (a multiple of --layers)")
+    p.add_argument("--warmup", type=int, default=72, help="layer-steps run before timing")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--rotate", type=int, default=4, help="independent buffer sets cycled to defeat L2")
+    p.add_argument("--layers", type=int, default=36,
+                   help="layers per decode step (Qwen3-8B has 36); each has its own buffers")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (CPU baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -253,8 +254,11 @@ def run_ours(args):
     okv.load()
     w = wl.WORKLOADS[WORKLOAD_ID]
     dev = torch.device("cuda", local)
+    R = max(1, args.layers)
 
-    # ---- setup (untimed): KV cache, summaries, prior tables, pool, pinned host tier
+    # ---- setup (untimed): KV cache, summaries, prior tables, pool, pinned host tier.
+    # Every layer gets its own device buffers (summaries, pool, tables, outputs) filled
+    # from the same synthetic layer; the host tier is shared.
     tiles = torch.empty((w.S, w.Nb, 2, 16, w.D), dtype=torch.bfloat16, device=dev)
     for s0 in range(0, w.S, 8):
         tiles[s0:s0 + 8] = wl.kv_tiles(w, 0, list(range(s0, min(w.S, s0 + 8))), device=dev)
@@ -264,67 +268,78 @@ def run_ours(args):
     q = wl.q_true(w, 0).to(dev)
     qd = wl.drafts(w, 0).to(dev)
     shape = okv.LayerShape(B=w.B, Hkv=w.Hkv, G=w.G, D=w.D, Nb_max=w.Nb, K=w.K, W=w.W, cap=w.cap, Nd=w.Nd)
-    insts = []
     strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
-    for i in range(args.rotate):
+    insts = []
+    for i in range(R):
         lay = okv.DecodeLayer(shape, device=dev)
         lay.build_summary(tiles, sl, 0, w.Nb, strides=strides)
         insts.append(lay)
     table0 = _gpu_prior(w, insts[0], tiles, sl, q).to(dev)
-    idx = table0.long().clamp(min=0)
-    pool0 = tiles[torch.arange(w.S, device=dev)[:, None], idx]
+    pool0 = tiles[torch.arange(w.S, device=dev)[:, None], table0.long().clamp(min=0)]
     for lay in insts:
         lay.table.copy_(table0)
         lay.pool.copy_(pool0)
+    del pool0
     new_keys = tiles[:, w.Nb - 1:w.Nb, 0].contiguous()     # keys of the newest block, [S][1][16][D]
     seg_stride = host[0].numel() * 2
     torch.cuda.synchronize()
-    del pool0
-
-    graphs = [okv.StepGraph(lay, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1)
-              for lay in insts]
-    R = len(graphs)
-    rounds = max(1, (args.steps + R - 1) // R)
-    steps = rounds * R
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(max(1, (args.warmup + R - 1) // R)):
-        for g in graphs:
-            g.replay()
+    def time_replays(replay, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n                       # ms per replay
+
+    # ---- the timed region: decode steps through R layers, one CUDA graph each
+    step_graph = okv.DecodeStepGraph(insts, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys,
+                                     new_block=w.Nb - 1)
+    reps = max(1, -(-args.steps // R))
+    layer_steps = reps * R
+    for _ in range(max(1, -(-args.warmup // R))):
+        step_graph.replay()
     barrier()
     clocks = ClockSampler(local) if rank == 0 else None
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.nvtx.range_push("oasis_timed")
     e0.record()
-    for _ in range(rounds):
-        for g in graphs:
-            g.replay()
+    for _ in range(reps):
+        step_graph.replay()
     e1.record()
     torch.cuda.nvtx.range_pop()
     barrier()
     clk = clocks.stop() if clocks else None
-    ms = e0.elapsed_time(e1) / steps
+    ms = e0.elapsed_time(e1) / layer_steps                  # per layer-step
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    assert insts[0].status.item() == 0, okv.strerror(insts[0].status.item())
+    st = torch.stack([lay.status for lay in insts]).max().item()
+    assert st == 0, okv.strerror(int(st))
 
-    # per-kernel durations: a CUDA graph of back-to-back launches of one kernel
-    # over the rotating buffer sets, replayed between events on the replay stream
+    # ---- one layer alone (no pipelining across layers): a StepGraph per buffer set
+    iso = [okv.StepGraph(lay, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1)
+           for lay in insts[:4]]
+    iso_ms = time_replays(lambda: [g.replay() for g in iso], 100) / len(iso)
+
+    # ---- per-kernel durations: a CUDA graph of back-to-back launches of one kernel
+    # over the layers' buffer sets, replayed between events on the replay stream
     kern = {}
-    calls = {"score": lambda lay, st: lay.score(qd, sl, stream=st),
-             "attn": lambda lay, st: lay.attend(q, sl, stream=st),
-             "select": lambda lay, st: lay.select(sl, stream=st),
-             "stage": lambda lay, st: lay.stage(host, seg_stride, w.Nb, stream=st),
-             "summary_update": lambda lay, st: lay.build_summary(new_keys, sl, blk_begin=w.Nb - 1, blk_count=1,
-                                                                 stream=st)}
-    n_launch = 4 * R
+    calls = {"score": lambda lay, st_: lay.score(qd, sl, stream=st_),
+             "attn": lambda lay, st_: lay.attend(q, sl, stream=st_),
+             "select": lambda lay, st_: lay.select(sl, stream=st_),
+             "stage": lambda lay, st_: lay.stage(host, seg_stride, w.Nb, stream=st_),
+             "summary_update": lambda lay, st_: lay.build_summary(new_keys, sl, blk_begin=w.Nb - 1, blk_count=1,
+                                                                  stream=st_)}
+    n_launch = max(8, R)
     for name, fn in calls.items():
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -334,16 +349,10 @@ def run_ours(args):
                 fn(insts[i % R], side)
         kg.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 20
         torch.cuda.nvtx.range_push(f"oasis_kernel_{name}")
-        a.record()
-        for _ in range(reps):
-            kg.replay()
-        b.record()
+        kern[name] = time_replays(kg.replay, 20) / n_launch * 1e3          # us per launch
         torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize()
-        kern[name] = a.elapsed_time(b) / (reps * n_launch) * 1e3      # us per launch
+
     per_layer = w.headline_bytes_per_layer()
     value = per_layer * world / (ms / 1e3) / 1e9
     peak, peak_kind = _peaks()
@@ -351,68 +360,86 @@ def run_ours(args):
     attn_bytes = w.kv_bytes_per_layer() + w.out_bytes_per_layer()
     k_gbs = {"score": score_bytes / (kern["score"] * 1e-6) / 1e9, "attn": attn_bytes / (kern["attn"] * 1e-6) / 1e9}
     dom = "attn" if kern["attn"] >= kern["score"] else "score"
+    kname = {"attn": "k_attn", "score": "k_score"}
     roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": "k_score (oasis_score_blocks)"}[dom],
             "bound": "hbm", "achieved": k_gbs[dom], "peak": peak, "unit": "GB/s", "frac": k_gbs[dom] / peak,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-            "traffic": None,
+            "traffic": _traffic(kname[dom]),
             "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes,
-            "timing": "CUDA graph of back-to-back launches over the rotating buffer sets, CUDA events",
-            "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak} for k in k_gbs if k != dom}}
+            "timing": "CUDA graph of back-to-back launches over the layers' buffer sets, CUDA events",
+            "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak, "traffic": _traffic(kname[k])}
+                      for k in k_gbs if k != dom}}
 
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev)
-
+        e2e = _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time_replays)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = _cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": steps,
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": layer_steps,
                 "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": _config(w, {"l2": f"{len(insts)} rotating buffer sets "
-                                            f"({len(insts) * per_layer / 1e6:.0f} MB of step inputs > L2)",
-                                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-                "roofline": roof, "kernels_us": kern, "gpu_launches": 5 * steps,
+                "config": _config(w, {
+                    "layers_per_decode_step": R,
+                    "step": "one pass of the whole path (summary update, scoring, capped selection, staging, "
+                            "attention) over one layer; decode steps of R such layers run as one CUDA graph, "
+                            "layer-pipelined (background of layer l overlaps the attention of later layers)",
+                    "l2": f"{R} per-layer buffer sets ({R * per_layer / 1e9:.1f} GB of step inputs > L2)",
+                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+                "single_layer_step_us": iso_ms * 1e3,
+                "roofline": roof, "kernels_us": kern, "gpu_launches": 5 * layer_steps,
                 "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev):
-    """Same metric through the public step call with host buffers: every step
-    is one StepGraph replay that copies the step's inputs (queries, drafts,
-    lengths, newest block's keys) from pinned host memory, runs the step and
-    copies its results (outputs, lse, new table, plan, counts) back."""
+def _traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel's current source (else None)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "sparse_kv_cache_quest_gb300", "csrc", rec["source"])
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+            return None
+    return rec["dram_bytes_per_launch"]
+
+
+def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time_replays):
+    """Same metric through the public call with host buffers: every decode step
+    is one DecodeStepGraph(host_io=True) replay that copies each layer's inputs
+    (queries, drafts, newest block's keys) from pinned host memory, runs the R
+    layers and copies each layer's results (outputs, lse, new table, plan,
+    counts) back to pinned host memory."""
     import torch
     import torch.distributed as dist
 
     import sparse_kv_cache_quest_gb300 as okv
-    graphs = [okv.StepGraph(lay, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
-                            host_io=True) for lay in insts]
-    R = len(graphs)
-    rounds = max(1, (args.steps + R - 1) // R)
-    for g in graphs:
-        g.replay()
+    g = okv.DecodeStepGraph(insts, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
+                            host_io=True)
+    R = len(insts)
+    g.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(rounds):
-        for g in graphs:
-            g.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (rounds * R)
+    reps = max(1, min(200, -(-args.steps // R)))
+    ms = time_replays(g.replay, reps) / R
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return {"value": w.headline_bytes_per_layer() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": graphs[0].h2d_bytes, "d2h_bytes_per_step": graphs[0].d2h_bytes,
-            "how": "StepGraph(host_io=True).replay(): H2D inputs + step + D2H results per step"}
+            "h2d_bytes_per_step": g.h2d_bytes // R, "d2h_bytes_per_step": g.d2h_bytes // R,
+            "how": "DecodeStepGraph(host_io=True).replay(): per layer-step H2D of its inputs, the step, "
+                   "D2H of its results"}
 
 
 def main():

@@ -195,10 +195,12 @@ int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int h
  * over every valid token i of every slot whose table entry is >= 0.
  * out: float32 [B][Hq][D].  lse (may be NULL): float32 [B][Hq], the natural
  * log of sum_i exp(scale * q . k_i).  No valid token: out = 0, lse = -inf.
- * fp32 accumulation; against a float64 evaluation the error is within 1e-2
+ * Products on the tensor cores with fp32 accumulation (p is carried as a
+ * bf16 hi + lo pair); against a float64 evaluation the error is within 1e-2
  * max-abs and 1e-3 relative L2 on N(0,1)-like bf16 data.
  * EINVAL: a NULL or misaligned pointer, D not 64 or 128, G not in [1, 16],
- * B or Hkv < 1, slots_per_seg not in [1, 4096].  status may be NULL.
+ * B or Hkv < 1, slots_per_seg not in [1, 4096], B*Hkv*slots_per_seg*32 >= 2^31
+ * (pool rows).  status may be NULL.
  */
 int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
                              const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,

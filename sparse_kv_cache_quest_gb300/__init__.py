@@ -8,4 +8,4 @@ from .binding import (  # noqa: F401
     EXPORTS, OasisError, abi_version, load, oasis_build_summary, oasis_score_blocks,
     oasis_select_topk_capped, oasis_sparse_decode_attn, oasis_stage_blocks, strerror,
 )
-from .layer import DecodeLayer, LayerShape, StepGraph  # noqa: F401
+from .layer import DecodeLayer, DecodeStepGraph, LayerShape, StepGraph  # noqa: F401

@@ -138,7 +138,7 @@ int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int3
   if (!q || !pool || !table || !seq_len || !out) return OASIS_EINVAL;
   if (!d_ok(D) || !segs_ok(B, Hkv) || G < 1 || G > 16 || slots_per_seg < 1 || slots_per_seg > 4096)
     return OASIS_EINVAL;
-  if (static_cast<int64_t>(B) * Hkv * ((G + 7) / 8) > 65535) return OASIS_EINVAL;
+  if (static_cast<int64_t>(B) * Hkv * slots_per_seg * 32 > 0x7FFFFFFF) return OASIS_EINVAL;  // pool rows
   if (!aligned16(q) || !aligned16(pool) || !aligned4(table) || !aligned4(seq_len) || !aligned4(out))
     return OASIS_EINVAL;
   if ((lse && !aligned4(lse)) || (status && !aligned4(status))) return OASIS_EINVAL;

@@ -7,39 +7,36 @@
 //     out = sum_i softmax_i(scale * q . k_i) v_i
 // over the valid tokens of the slots whose table entry is >= 0.
 //
-// Data path.  A segment's pool is slots_per_seg contiguous 8 KiB tiles (K then
-// V, D = 128).  The segment is split over a thread-block cluster of CL CTAs
-// (split-K): the CL*4 warps of the cluster take the slots round-robin.  Each
-// warp first lists its non-empty slots in shared memory (one table read per
-// slot, off the streaming loop), then streams their tiles through a ring of
-// NST shared-memory stages with 1-D bulk async copies (cp.async.bulk, one
-// mbarrier per stage, lane 0 issues), so the next tile is in flight while one
-// is consumed.  Empty slots and slots without valid tokens are never loaded.
+// Data path.  A segment's pool is slots_per_seg contiguous 8 KiB tiles (16
+// key rows, then 16 value rows, D = 128).  The segment is split over a
+// thread-block cluster of CL CTAs (split-K); the CL*4 warps of the cluster
+// take the slots round-robin.  Each warp first lists its non-empty slots in
+// shared memory (one table read per slot), then streams their tiles through a
+// private two-stage ring with 2-D TMA tensor copies (cp.async.bulk.tensor, one
+// mbarrier per stage, lane 0 issues).  The tensor map views the pool as rows
+// of D bf16 and uses the 128-byte swizzle, so the tensor-core fragment loads
+// below are bank-conflict free.  Empty slots are never loaded.
 //
-// Math (CUDA cores: a GQA group of a few heads is no dense tensor-core tile).
-// A warp works on one 16-token slot at a time.  Lane (tsub = lane/16,
-// dpart = lane%16) owns dims dpart*VEC .. +VEC of tokens 2u + tsub (u < 8).
-//  * QK: per lane, partial dots of its dims for its 8 tokens and the GT query
-//    heads, two heads per packed fp32x2 FMA.  The lane visits its tokens in the
-//    order u_i = i ^ rot (rot = dpart bits 3..1) and holds its heads in the
-//    order g_k = k ^ (dpart bit 0) * GT/2, so that a butterfly reduce-scatter
-//    over the 16 lanes of a half (xor 8, 4, 2 over tokens, xor 1 over heads)
-//    always exchanges registers with static indices (GT*7 + GT/2 shuffles
-//    instead of an all-reduce's 32*GT); afterwards each lane owns the complete
-//    logits of token 2*rot + tsub for heads g_0 .. g_{GT/2-1}.
-//  * Online softmax in the log2 domain (q pre-scaled by scale*log2(e), exp2f)
-//    on the owned logits only; running max m and sum l per head.
-//  * PV: each lane gathers p for its 8 tokens and GT heads with shuffles and
-//    accumulates o[g][its dims] with packed fp32x2 FMAs over dim pairs.
+// Math, per warp and 16-token slot, on the tensor cores (mma.sync m16n8k16,
+// bf16 inputs, fp32 accumulation):
+//   S^T[16 tokens x 8n queries] = K[16 x D] . Q^T[D x 8n]   (Q fragments in registers)
+//   online softmax over tokens in the log2 domain (scale*log2(e) applied in fp32)
+//   O^T[D x 8n] += V^T[D x 16] . P^T[16 x 8n]
+// The query heads of the GQA group fill the N dimension (8 or 16 columns; unused
+// columns are zero).  P^T reaches the B-fragment layout with one in-register
+// 8x8 transpose per half (movmatrix), and is split into bf16 hi + lo parts so
+// that the PV product keeps about 16 significant bits of p.  Each thread owns
+// whole output elements, so no cross-lane reduction is needed per slot.
 // Warps combine through shared memory (reusing the rings), then the CL CTAs of
 // the cluster combine through distributed shared memory into rank 0, which
 // writes out and lse.  No global scratch memory is used.
-//
-// G > 8 is processed in query-head tiles of 8 (separate clusters).
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cfloat>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -50,113 +47,133 @@ namespace {
 
 constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
+constexpr int kNST = 2;                    // ring stages per warp
+constexpr int kListMax = 512;              // listed slots per warp
 constexpr uint32_t kWaitTries = 1u << 22;  // bounded mbarrier polls (far beyond any real copy)
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Widen VEC bf16 (16 or 8 bytes of shared memory) to fp32.
-template <int VEC>
-__device__ __forceinline__ void load_row(const uint16_t *p, float (&f)[VEC]) {
-  if constexpr (VEC == 8) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(p);
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-  } else {
-    const uint2 v = *reinterpret_cast<const uint2 *>(p);
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-  }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += a . b  (m16n8k16, bf16 x bf16 -> fp32)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// {lo, hi} -> bf16x2 with `lo` in the low half (round to nearest even)
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
 }
 
-template <int VEC, int GT>
-struct Smem {
-  static constexpr int D = 16 * VEC;
-  static constexpr int kTile = 64 * D;  // bytes per slot tile
-  // combine scratch (floats), aliased onto the rings after the main loop
-  static constexpr int kWarpM = 0, kWarpL = kWarps * GT, kWarpO = 2 * kWarps * GT;
-  static constexpr int kCtaM = kWarpO + kWarps * GT * D, kCtaL = kCtaM + GT, kCtaO = kCtaL + GT;
-  static constexpr int kScratchFloats = kCtaO + GT * D;
+// Shared-memory plan (offsets in bytes from a 1024-aligned base).
+template <int D, int GQ>
+struct Plan {
+  static constexpr int kTile = 64 * D;                    // one slot: 32 rows of D bf16
+  static constexpr int kRing = kWarps * kNST * kTile;
+  static constexpr int kBars = kRing;                      // kWarps * kNST mbarriers
+  static constexpr int kLists = kBars + 8 * kWarps * kNST; // kWarps * kListMax int32
+  static constexpr int kEnd = kLists + 4 * kWarps * kListMax;
+  // combine scratch (floats), aliased onto the ring once every stage is drained
+  static constexpr int kWarpM = 0, kWarpL = kWarps * GQ, kWarpO = 2 * kWarps * GQ;
+  static constexpr int kCtaM = kWarpO + kWarps * GQ * D, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
+  static constexpr int kScratchBytes = 4 * (kCtaO + GQ * D);
+  static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
 
-template <int VEC, int GT, int NST>
+// KS = D / 16 (k-steps of the QK product and m-tiles of the PV product);
+// NT = query tiles of 8 heads (GQ = 8 * NT columns).
+template <int KS, int NT>
 __global__ void __launch_bounds__(kThreads)
-    k_attn(const uint16_t *__restrict__ q, const uint16_t *__restrict__ pool, const int32_t *__restrict__ table,
-           int slots, const int32_t *__restrict__ seq_len, int Hkv, int G, int ntiles, float scale_log2,
-           float *__restrict__ out, float *__restrict__ lse, int32_t *status, int list_cap) {
-  using SM = Smem<VEC, GT>;
-  constexpr int D = SM::D;
-  constexpr uint32_t kTileBytes = SM::kTile;
-  constexpr int H = GT > 1 ? GT / 2 : 1;  // heads owned per lane after the reduce-scatter
-  extern __shared__ __align__(128) unsigned char sm[];
+    k_attn(const __grid_constant__ CUtensorMap tmap, const uint16_t *__restrict__ q,
+           const int32_t *__restrict__ table, int slots, const int32_t *__restrict__ seq_len, int Hkv, int G,
+           float scale_log2, float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
+  constexpr int D = 16 * KS;
+  constexpr int GQ = 8 * NT;
+  constexpr int kBoxes = D / 64;  // 64-dim boxes (128 bytes per row) per tile
+  using P = Plan<D, GQ>;
+  extern __shared__ unsigned char sm_raw[];
+  const uint32_t raw_addr = smem_addr(sm_raw);
+  unsigned char *sm = sm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(sm);
   cg::cluster_group cluster = cg::this_cluster();
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tsub = lane >> 4, dpart = lane & 15;
-  const int rot = (dpart >> 1) & 7;  // token order u_i = i ^ rot
-  const int hb = dpart & 1;          // head order  g_k = k ^ hb * GT/2
+  const int g = lane >> 2, t = lane & 3;
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int s = blockIdx.y / ntiles, tile = blockIdx.y % ntiles;
+  const int s = blockIdx.y;
   const int bseq = s / Hkv, h = s % Hkv;
-  const int g0 = tile * GT;
-  const int gcount = min(GT, G - g0);
   const int Hq = Hkv * G;
 
   int L = seq_len[bseq];
   if (L < 0) {
-    if (tid == 0 && rank == 0 && h == 0 && tile == 0) report(status, OASIS_STATUS_SEQ_LEN);
+    if (tid == 0 && rank == 0 && h == 0) report(status, OASIS_STATUS_SEQ_LEN);
     L = 0;
   }
-
-  unsigned char *ring = sm + static_cast<size_t>(warp) * NST * kTileBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + static_cast<size_t>(kWarps) * NST * kTileBytes) + warp * NST;
-  float *scratch = reinterpret_cast<float *>(sm);  // used only once every ring stage is drained
-  int32_t *list = reinterpret_cast<int32_t *>(bars + (kWarps - warp) * NST) + warp * list_cap;
-
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + P::kBars) + warp * kNST;
+  int32_t *list = reinterpret_cast<int32_t *>(sm + P::kLists) + warp * kListMax;
+  const uint32_t ring = sbase + warp * kNST * P::kTile;
   if (lane == 0) {
-    for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNST; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
-  __syncwarp();
 
-  // query slot k holds head g_k = k ^ (hb * GT/2); packed in head pairs for fp32x2
-  unsigned long long q2[(GT + 1) / 2][VEC];
-  {
-    float qf[GT][VEC];
+  // Q^T B-fragments: column n = query head nt*8 + g, rows k = dims 16ks + 2t (+1, +8, +9)
+  uint32_t qb[NT][KS][2];
 #pragma unroll
-    for (int k = 0; k < GT; ++k) {
-      const int g = GT > 1 ? (k ^ (hb * (GT / 2))) : 0;
-      if (g < gcount) {
-        float f[VEC];
-        load_row<VEC>(q + (static_cast<int64_t>(bseq) * Hq + h * G + g0 + g) * D + dpart * VEC, f);
+  for (int nt = 0; nt < NT; ++nt) {
+    const int qi = nt * 8 + g;
+    const uint32_t *row =
+        reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bseq) * Hq + h * G + qi) * D);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) qf[k][e] = f[e] * scale_log2;
-      } else {
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[nt][ks][0] = qi < G ? row[(16 * ks + 2 * t) >> 1] : 0u;
+      qb[nt][ks][1] = qi < G ? row[(16 * ks + 8 + 2 * t) >> 1] : 0u;
+    }
+  }
+  float o[NT][KS][4];
+  float m[NT][2], l[NT][2];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) qf[k][e] = 0.0f;
-      }
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      m[nt][j] = -INFINITY;
+      l[nt][j] = 0.0f;
     }
 #pragma unroll
-    for (int kp = 0; kp < (GT + 1) / 2; ++kp)
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) q2[kp][e] = pack2(qf[2 * kp][e], 2 * kp + 1 < GT ? qf[2 * kp + 1][e] : 0.0f);
+      for (int i = 0; i < 4; ++i) o[nt][mt][i] = 0.0f;
   }
-  float m[GT], l[H];
-  unsigned long long o2[GT][VEC / 2];  // o[k][e], dims packed in pairs
-#pragma unroll
-  for (int k = 0; k < GT; ++k) {
-    m[k] = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < VEC / 2; ++e) o2[k][e] = 0ull;
-  }
-#pragma unroll
-  for (int k = 0; k < H; ++k) l[k] = 0.0f;
 
-  // this warp's slots: gw, gw + nw, ... over the whole cluster; the non-empty ones
-  // (slot << 5 | valid tokens) go to a per-warp list in shared memory, so the
-  // streaming loop below makes no global-memory round trip for control flow
+  // this warp's non-empty slots, as (slot << 5 | valid tokens)
   const int nw = CL * kWarps, gw = rank * kWarps + warp;
   const int nk = slots > gw ? (slots - gw + nw - 1) / nw : 0;
   const int32_t *trow = table + static_cast<int64_t>(s) * slots;
-  const uint16_t *prow = pool + static_cast<int64_t>(s) * slots * 32 * D;
   int count = 0;
   for (int base = 0; base < nk; base += 32) {
     const int k = base + lane;
@@ -172,110 +189,103 @@ __global__ void __launch_bounds__(kThreads)
     count += __popc(mk);
   }
   __syncwarp();
+  const int row_base = s * slots;  // tile index of slot 0 of this segment
   auto issue = [&](int c, int stg) {
-    mbar_arrive_expect_tx(&bars[stg], kTileBytes);
-    bulk_g2s(ring + stg * kTileBytes, prow + static_cast<int64_t>(list[c] >> 5) * 32 * D, kTileBytes, &bars[stg]);
+    mbar_arrive_expect_tx(&bars[stg], P::kTile);
+    const int y = (row_base + (list[c] >> 5)) * 32;
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_load_2d(ring + stg * P::kTile + bx * 4096, &tmap, bx * 64, y, &bars[stg]);
   };
   if (lane == 0)
-    for (int c = 0; c < NST && c < count; ++c) issue(c, c);
-  int issued = min(NST, count), consumed = 0;
+    for (int c = 0; c < kNST && c < count; ++c) issue(c, c);
+  int issued = min(kNST, count), consumed = 0;
   bool timed_out = false;
+
+  // fragment addressing inside a swizzled tile: row r, 16-byte chunk j of the D-wide row
+  auto frag_addr = [&](uint32_t tile, int r, int j) {
+    return tile + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4);
+  };
+  const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);  // K rows 0..15 for ldmatrix
+  const int khalf = lane >> 4;
+  const int vrow = 16 + (lane & 7) + 8 * (lane >> 4);   // V rows 16..31 for ldmatrix.trans
+  const int vhalf = (lane >> 3) & 1;
+
   for (int c = 0; c < count; ++c) {
-    const int stg = c % NST;
-    const bool ok = mbar_wait_bounded(&bars[stg], static_cast<uint32_t>(c / NST) & 1u, kWaitTries);
+    const int stg = c % kNST;
+    const bool ok = mbar_wait_bounded(&bars[stg], static_cast<uint32_t>(c / kNST) & 1u, kWaitTries);
     if (__any_sync(0xFFFFFFFFu, !ok)) {
       timed_out = true;
       break;
     }
     const int nv = list[c] & 31;
-    const uint16_t *kt = reinterpret_cast<const uint16_t *>(ring + stg * kTileBytes);
-    const uint16_t *vt = kt + kBlockTokens * D;
+    const uint32_t tile = ring + stg * P::kTile;
 
-    // ---- QK partials: sc[k][i] for head slot k, token u_i = i ^ rot
-    float sc[GT][8];
+    // ---- S^T = K . Q^T
+    float sacc[NT][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float kf[VEC];
-      load_row<VEC>(kt + (2 * (i ^ rot) + tsub) * D + dpart * VEC, kf);
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int kp = 0; kp < (GT + 1) / 2; ++kp) {
-        unsigned long long a = 0ull;
+      for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.0f;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) a = fma2(q2[kp][e], pack2(kf[e], kf[e]), a);
-        float a0, a1;
-        unpack2(a, a0, a1);
-        sc[2 * kp][i] = a0;
-        if (2 * kp + 1 < GT) sc[2 * kp + 1][i] = a1;
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      ldsm_x4(frag_addr(tile, krow, 2 * ks + khalf), a);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816(sacc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+    }
+    // ---- online softmax over the slot's tokens (rows g and g + 8), per query column
+    const bool v0 = g < nv, v1 = g + 8 < nv;
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float p0[2], p1[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float x0 = v0 ? sacc[nt][j] * scale_log2 : -INFINITY;
+        const float x1 = v1 ? sacc[nt][2 + j] * scale_log2 : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const float mn = fmaxf(m[nt][j], mx);
+        const float corr = exp2f(m[nt][j] - mn);
+        m[nt][j] = mn;
+        p0[j] = exp2f(x0 - mn);
+        p1[j] = exp2f(x1 - mn);
+        l[nt][j] = l[nt][j] * corr + p0[j] + p1[j];
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[nt][mt][j] *= corr;
+          o[nt][mt][2 + j] *= corr;
+        }
       }
+      // P^T B-fragments: hi and lo bf16 parts, transposed 8x8 per token half
+      const uint32_t h0 = pack_bf16(p0[0], p0[1]), h1 = pack_bf16(p1[0], p1[1]);
+      const uint32_t l0 = pack_bf16(p0[0] - bf16_lo(h0), p0[1] - bf16_hi(h0));
+      const uint32_t l1 = pack_bf16(p1[0] - bf16_lo(h1), p1[1] - bf16_hi(h1));
+      bh[nt][0] = transpose8x8(h0);
+      bh[nt][1] = transpose8x8(h1);
+      bl[nt][0] = transpose8x8(l0);
+      bl[nt][1] = transpose8x8(l1);
     }
-    // ---- reduce-scatter over the 16 lanes of the half
+    // ---- O^T += V^T . P^T
 #pragma unroll
-    for (int k = 0; k < GT; ++k) {
+    for (int mt = 0; mt < KS; ++mt) {
+      uint32_t a[4];
+      ldsm_x4_t(frag_addr(tile, vrow, 2 * mt + vhalf), a);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sc[k][j] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][j + 4], 8);
-#pragma unroll
-      for (int j = 0; j < 2; ++j) sc[k][j] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][j + 2], 4);
-      sc[k][0] += __shfl_xor_sync(0xFFFFFFFFu, sc[k][1], 2);
-    }
-    float s_own[H];
-    if constexpr (GT > 1) {
-#pragma unroll
-      for (int k = 0; k < H; ++k) s_own[k] = sc[k][0] + __shfl_xor_sync(0xFFFFFFFFu, sc[k + H][0], 1);
-    } else {
-      s_own[0] = sc[0][0] + __shfl_xor_sync(0xFFFFFFFFu, sc[0][0], 1);
-    }
-    const bool tok_ok = 2 * rot + tsub < nv;
-    // ---- online softmax on the owned logits
-    float mnew[GT];
-#pragma unroll
-    for (int k = 0; k < H; ++k) {
-      float v = tok_ok ? s_own[k] : -INFINITY;
-      s_own[k] = v;
-      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 16));
-      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
-      mnew[k] = fmaxf(m[k], v);
-    }
-    if constexpr (GT > 1) {
-#pragma unroll
-      for (int k = 0; k < H; ++k) mnew[k + H] = __shfl_xor_sync(0xFFFFFFFFu, mnew[k], 1);
-    }
-    float p_own[H];
-#pragma unroll
-    for (int k = 0; k < H; ++k) {
-      p_own[k] = exp2f(s_own[k] - mnew[k]);
-      const float lcorr = exp2f(m[k] - mnew[k]);
-      l[k] = l[k] * lcorr + ((GT > 1 || hb == 0) ? p_own[k] : 0.0f);
-    }
-#pragma unroll
-    for (int k = 0; k < GT; ++k) {
-      const float corr = exp2f(m[k] - mnew[k]);
-      const unsigned long long c2 = pack2(corr, corr);
-#pragma unroll
-      for (int e = 0; e < VEC / 2; ++e) o2[k][e] = fma2(o2[k][e], c2, 0ull);
-      m[k] = mnew[k];
-    }
-    // ---- PV: gather p of this lane's tokens, accumulate its dims
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      float vf[VEC];
-      load_row<VEC>(vt + (2 * u + tsub) * D + dpart * VEC, vf);
-#pragma unroll
-      for (int k = 0; k < GT; ++k) {
-        const int src = tsub * 16 + 2 * u + (GT > 1 ? ((k >= H) ^ hb) : 0);
-        const float p = __shfl_sync(0xFFFFFFFFu, p_own[GT > 1 ? k % H : 0], src);
-        const unsigned long long p2 = pack2(p, p);
-#pragma unroll
-        for (int e = 0; e < VEC / 2; ++e) o2[k][e] = fma2(p2, pack2(vf[2 * e], vf[2 * e + 1]), o2[k][e]);
+      for (int nt = 0; nt < NT; ++nt) {
+        mma16816(o[nt][mt], a, bh[nt][0], bh[nt][1]);
+        mma16816(o[nt][mt], a, bl[nt][0], bl[nt][1]);
       }
     }
     __syncwarp();
     ++consumed;
-    if (c + NST < count) {
+    if (c + kNST < count) {
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue(c + NST, stg);
+        issue(c + kNST, stg);
       }
       ++issued;
     }
@@ -283,92 +293,78 @@ __global__ void __launch_bounds__(kThreads)
   if (timed_out) {
     if (lane == 0) report(status, OASIS_STATUS_TIMEOUT);
     for (int c = consumed; c < issued; ++c)
-      mbar_wait_bounded(&bars[c % NST], static_cast<uint32_t>(c / NST) & 1u, kWaitTries);
+      mbar_wait_bounded(&bars[c % kNST], static_cast<uint32_t>(c / kNST) & 1u, kWaitTries);
   }
 
-  // ---- per-warp totals: l over the owning lanes, o over the two token halves
+  // ---- warp totals: l over the token rows (lanes with equal t); o is complete per thread
 #pragma unroll
-  for (int k = 0; k < H; ++k) {
-    float v = l[k];
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
-    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-    if constexpr (GT == 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    l[k] = v;
-  }
-  float lfull[GT];
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-  for (int k = 0; k < H; ++k) lfull[k] = l[k];
-  if constexpr (GT > 1) {
-#pragma unroll
-    for (int k = 0; k < H; ++k) lfull[k + H] = __shfl_xor_sync(0xFFFFFFFFu, l[k], 1);
-  }
-  float of[GT][VEC];
-#pragma unroll
-  for (int k = 0; k < GT; ++k)
-#pragma unroll
-    for (int e = 0; e < VEC / 2; ++e) {
-      float a, b;
-      unpack2(o2[k][e], a, b);
-      of[k][2 * e] = a + __shfl_xor_sync(0xFFFFFFFFu, a, 16);
-      of[k][2 * e + 1] = b + __shfl_xor_sync(0xFFFFFFFFu, b, 16);
+    for (int j = 0; j < 2; ++j) {
+      float v = l[nt][j];
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+      v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+      l[nt][j] = v;
     }
   __syncthreads();  // every warp is past its ring: the scratch may alias it
-  float *wm = scratch + SM::kWarpM, *wl = scratch + SM::kWarpL, *wo = scratch + SM::kWarpO;
-  float *cm = scratch + SM::kCtaM, *cl = scratch + SM::kCtaL, *co = scratch + SM::kCtaO;
-  if (lane == 0) {  // hb = 0 here: slot k holds head k
+  float *scratch = reinterpret_cast<float *>(sm);
+  float *wm = scratch + P::kWarpM, *wl = scratch + P::kWarpL, *wo = scratch + P::kWarpO;
+  float *cm = scratch + P::kCtaM, *cl = scratch + P::kCtaL, *co = scratch + P::kCtaO;
 #pragma unroll
-    for (int k = 0; k < GT; ++k) {
-      wm[warp * GT + k] = m[k];
-      wl[warp * GT + k] = lfull[k];
+  for (int nt = 0; nt < NT; ++nt) {
+    if (g == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        wm[warp * GQ + nt * 8 + 2 * t + j] = m[nt][j];
+        wl[warp * GQ + nt * 8 + 2 * t + j] = l[nt][j];
+      }
     }
-  }
-  if (tsub == 0) {
 #pragma unroll
-    for (int k = 0; k < GT; ++k) {
-      const int g = GT > 1 ? (k ^ (hb * (GT / 2))) : 0;
+    for (int mt = 0; mt < KS; ++mt)
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) wo[(warp * GT + g) * D + dpart * VEC + e] = of[k][e];
-    }
+      for (int i = 0; i < 4; ++i) {
+        const int qc = nt * 8 + 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
+        wo[(warp * GQ + qc) * D + dim] = o[nt][mt][i];
+      }
   }
   __syncthreads();
-  for (int idx = tid; idx < GT * D; idx += kThreads) {
-    const int g = idx / D, d = idx % D;
+  for (int idx = tid; idx < GQ * D; idx += kThreads) {
+    const int qc = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * GT + g]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * GQ + qc]);
     float acc = 0.0f, ls = 0.0f;
     if (M > -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(wm[w * GT + g] - M);
-        acc += f * wo[(w * GT + g) * D + d];
-        ls += f * wl[w * GT + g];
+        const float f = exp2f(wm[w * GQ + qc] - M);
+        acc += f * wo[(w * GQ + qc) * D + d];
+        ls += f * wl[w * GQ + qc];
       }
     }
-    co[g * D + d] = acc;
+    co[qc * D + d] = acc;
     if (d == 0) {
-      cm[g] = M;
-      cl[g] = ls;
+      cm[qc] = M;
+      cl[qc] = ls;
     }
   }
   cluster.sync();
   if (rank == 0) {
-    for (int idx = tid; idx < GT * D; idx += kThreads) {
-      const int g = idx / D, d = idx % D;
-      if (g >= gcount) continue;
+    for (int idx = tid; idx < GQ * D; idx += kThreads) {
+      const int qc = idx / D, d = idx % D;
+      if (qc >= G) continue;
       float M = -INFINITY;
-      for (int r = 0; r < CL; ++r) M = fmaxf(M, cluster.map_shared_rank(cm, r)[g]);
+      for (int r = 0; r < CL; ++r) M = fmaxf(M, cluster.map_shared_rank(cm, r)[qc]);
       float acc = 0.0f, ls = 0.0f;
       if (M > -INFINITY) {
         for (int r = 0; r < CL; ++r) {
-          const float f = exp2f(cluster.map_shared_rank(cm, r)[g] - M);
-          acc += f * cluster.map_shared_rank(co, r)[g * D + d];
-          ls += f * cluster.map_shared_rank(cl, r)[g];
+          const float f = exp2f(cluster.map_shared_rank(cm, r)[qc] - M);
+          acc += f * cluster.map_shared_rank(co, r)[qc * D + d];
+          ls += f * cluster.map_shared_rank(cl, r)[qc];
         }
       }
-      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + g0 + g;
+      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
       out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
       if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
     }
@@ -376,30 +372,50 @@ __global__ void __launch_bounds__(kThreads)
   cluster.sync();
 }
 
-template <int VEC, int GT, int NST>
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <int KS, int NT>
 cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                      const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
                      int32_t *status, cudaStream_t st) {
-  using SM = Smem<VEC, GT>;
-  const int ntiles = (G + GT - 1) / GT;
-  const int units = B * Hkv * ntiles;
-  const size_t ring = static_cast<size_t>(kWarps) * NST * SM::kTile + sizeof(uint64_t) * kWarps * NST;
-  // the shared-memory size (and so the occupancy) is fixed by the rings; the slot
-  // lists take a fixed maximum of kListMax entries per warp
-  constexpr int kListMax = 512;
-  const size_t smem = std::max(ring + sizeof(int32_t) * kWarps * kListMax, sizeof(float) * SM::kScratchFloats);
+  constexpr int D = 16 * KS;
+  using P = Plan<D, 8 * NT>;
+  const int S = B * Hkv;
+  // the pool as a 2-D tensor: rows of D bf16, one 32-row box per 64 dims of a slot
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S) * slots * 32};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const size_t smem = P::kEnd + 1024;  // + slack for the 1024-byte alignment of the swizzled tiles
   int sms = 0, per_sm = 0;
-  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<VEC, GT, NST>), kThreads, smem, &sms,
-                                  &per_sm);
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<KS, NT>), kThreads, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
   // split every segment over a cluster so that the grid fills the resident CTA slots
-  int CL = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, static_cast<int64_t>(sms) * per_sm / units)));
+  int CL = static_cast<int>(std::min<int64_t>(8, std::max<int64_t>(1, static_cast<int64_t>(sms) * per_sm / S)));
   CL = std::min(CL, slots);
-  while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // keep each warp's list within kListMax
+  while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // each warp's list fits
   if (CL > 8) return cudaErrorInvalidValue;
-  const int list_cap = kListMax;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(CL), static_cast<unsigned>(units));
+  cfg.gridDim = dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -411,19 +427,8 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const float scale_log2 = scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, k_attn<VEC, GT, NST>, q, pool, table, slots, seq_len, Hkv, G, ntiles,
-                            scale_log2, out, lse, status, list_cap);
-}
-
-template <int VEC>
-cudaError_t launch_vec(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
-                       const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
-                       int32_t *status, cudaStream_t st) {
-  constexpr int NST = 2;
-  if (G == 1) return launch_t<VEC, 1, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
-  if (G == 2) return launch_t<VEC, 2, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
-  if (G <= 4) return launch_t<VEC, 4, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
-  return launch_t<VEC, 8, NST>(q, pool, table, slots, seq_len, B, Hkv, G, scale, out, lse, status, st);
+  return cudaLaunchKernelEx(&cfg, k_attn<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
+                            status);
 }
 
 }  // namespace
@@ -431,9 +436,12 @@ cudaError_t launch_vec(const uint16_t *q, const uint16_t *pool, const int32_t *t
 cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table,
                                       int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G, int D,
                                       float scale, float *out, float *lse, int32_t *status, cudaStream_t st) {
-  if (D == 128)
-    return launch_vec<8>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
-  return launch_vec<4>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+  if (D == 128) {
+    if (G <= 8) return launch_t<8, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+    return launch_t<8, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+  }
+  if (G <= 8) return launch_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+  return launch_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
 }
 
 }  // namespace oasis

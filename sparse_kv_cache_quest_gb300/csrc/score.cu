@@ -118,16 +118,21 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
           bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
           bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
         }
+      // unrolled by kPF only (ring indices stay compile-time constants): the fully
+      // unrolled body overflows the instruction cache
+#pragma unroll 1
+      for (int c0 = 0; c0 < CH; c0 += kPF)
 #pragma unroll
-      for (int c = 0; c < CH; ++c) {
+      for (int cc = 0; cc < kPF; ++cc) {
+        const int c = c0 + cc;
         uint4 mn[NB], mx[NB];
 #pragma unroll
         for (int i = 0; i < NB; ++i) {
-          mn[i] = bmn[c % kPF][i];
-          mx[i] = bmx[c % kPF][i];
+          mn[i] = bmn[cc][i];
+          mx[i] = bmx[cc][i];
           if (c + kPF < CH) {
-            bmn[c % kPF][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
-            bmx[c % kPF][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+            bmn[cc][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+            bmx[cc][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
           }
         }
         const float4 *qrow = qbase + (c * 8) * (NQP / 2);

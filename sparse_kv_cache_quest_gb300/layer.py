@@ -207,3 +207,93 @@ class StepGraph:
 
     def replay(self):
         self.graph.replay()
+
+
+class DecodeStepGraph:
+    """One decode step through several layers as one CUDA graph, pipelined
+    across layers as in the asynchronous prefetch pipeline of the OasisKV paper
+    review (xllm-io), §3 Fig. 8 and eq. (4): the foreground attends layer after
+    layer on one stream; the background of layer l (summary update + scoring,
+    then selection, then staging) starts once the foreground has reached layer l
+    (its draft queries exist) and overlaps the attention of the following
+    layers; the staging of layer l waits for layer l's attention (it overwrites
+    slots that attention reads) and must end before the next step, where the
+    graph ends.
+
+    Each layer gets static input buffers (q, qdraft, new_keys; seq_len is
+    shared); with host_io=True the graph first copies every layer's inputs from
+    pinned host staging tensors and ends by copying every layer's results
+    (out, lse, new table, plan, plan counts) back to pinned host memory.  Tables do not
+    advance (the new tables stay in ``table_next``).
+    """
+
+    def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
+                 new_block: Optional[int] = None, host_io: bool = False):
+        dev = layers[0].device
+        self.layers = layers
+        self.seq_len = seq_len.detach().to(dev).clone()
+        self.q = [q.detach().to(dev).clone() for _ in layers]
+        self.qdraft = [qdraft.detach().to(dev).clone() for _ in layers]
+        self.new_keys = [new_keys.detach().to(dev).contiguous().clone() if new_keys is not None else None
+                         for _ in layers]
+        ins = [[self.q[i], self.qdraft[i]] + ([self.new_keys[i]] if new_keys is not None else [])
+               for i in range(len(layers))]
+        outs = [[l.out, l.lse, l.table_next, l.plan, l.plan_count] for l in layers]
+        self.host_in = [[t.cpu().pin_memory() for t in x] for x in ins] if host_io else None
+        self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
+            if host_io else None
+        fg, bg, sel, xf = (torch.cuda.Stream(dev) for _ in range(4))
+        stage_args = (host_kv, host_seg_stride_bytes, host_nb)
+
+        def body(cur):
+            if host_io:
+                for i in range(len(layers)):
+                    for d, h in zip(ins[i], self.host_in[i]):
+                        d.copy_(h, non_blocking=True)
+            start = torch.cuda.Event()
+            start.record(cur)
+            for st in (fg, bg, sel, xf):
+                st.wait_event(start)
+            prev_fg = None
+            for i, lay in enumerate(layers):
+                if prev_fg is not None:
+                    bg.wait_event(prev_fg)                     # the forward pass has reached layer i
+                if new_keys is not None:
+                    lay.build_summary(self.new_keys[i], self.seq_len, blk_begin=new_block, blk_count=1, stream=bg)
+                lay.score(self.qdraft[i], self.seq_len, stream=bg)
+                e_sc = torch.cuda.Event()
+                e_sc.record(bg)
+                sel.wait_event(e_sc)
+                lay.select(self.seq_len, stream=sel)
+                e_sel = torch.cuda.Event()
+                e_sel.record(sel)
+                lay.attend(self.q[i], self.seq_len, stream=fg)
+                e_fg = torch.cuda.Event()
+                e_fg.record(fg)
+                prev_fg = e_fg
+                xf.wait_event(e_sel)
+                xf.wait_event(e_fg)
+                lay.stage(*stage_args, stream=xf)
+            for st in (fg, bg, sel, xf):
+                e = torch.cuda.Event()
+                e.record(st)
+                cur.wait_event(e)
+            if host_io:
+                for i in range(len(layers)):
+                    for h, d in zip(self.host_out[i], outs[i]):
+                        h.copy_(d, non_blocking=True)
+
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body(side)                                   # warm-up outside capture
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            body(side)
+        self.h2d_bytes = sum(t.numel() * t.element_size() for x in (self.host_in or []) for t in x)
+        self.d2h_bytes = sum(t.numel() * t.element_size() for x in (self.host_out or []) for t in x)
+
+    def replay(self):
+        self.graph.replay()
