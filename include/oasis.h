@@ -19,11 +19,10 @@
  *   oasis_sparse_decode_attn  attention of the true query over the slots
  *
  * Conventions shared by every entry point
- *   Memory.     The caller allocates and owns every buffer, including the
- *               attention workspace.  The library allocates no memory and
- *               keeps no state between calls (it only caches, per process and
- *               device, each kernel's launch geometry after raising its
- *               shared-memory limit).  Device pointers must be device memory or, where
+ *   Memory.     The caller allocates and owns every buffer.  The library
+ *               allocates no memory and keeps no state between calls (it only
+ *               caches, per process, that each kernel's shared-memory limit
+ *               was raised).  Device pointers must be device memory or, where
  *               stated, host memory the GPU can address (pinned and mapped).
  *   Execution.  Every call enqueues kernels on `stream` (NULL = the legacy
  *               default stream) and returns without synchronising.  Outputs
@@ -199,26 +198,13 @@ int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int h
  * Products on the tensor cores with fp32 accumulation (p is carried as a
  * bf16 hi + lo pair); against a float64 evaluation the error is within 1e-2
  * max-abs and 1e-3 relative L2 on N(0,1)-like bf16 data.
- * The slots of all segments are split evenly over the SMs; each part writes
- * a partial result (running max, sum, output) into the workspace `ws`, device
- * memory of at least oasis_attn_workspace_bytes(...) bytes, 16-byte aligned,
- * owned by the caller; a second kernel merges the partials.  The workspace
- * needs no initialisation and carries nothing between calls, but two calls
- * in flight at the same time must not share it.
- * EINVAL: a NULL or misaligned pointer (lse and status may be NULL), D not 64
- * or 128, G not in [1, 16], B or Hkv < 1, slots_per_seg not in [1, 4096],
- * B*Hkv*slots_per_seg*32 >= 2^31 (pool rows), ws_bytes too small.
+ * EINVAL: a NULL or misaligned pointer, D not 64 or 128, G not in [1, 16],
+ * B or Hkv < 1, slots_per_seg not in [1, 4096], B*Hkv*slots_per_seg*32 >= 2^31
+ * (pool rows).  status may be NULL.
  */
 int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
                              const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,
-                             float *out, float *lse, void *ws, size_t ws_bytes, int32_t *status,
-                             oasis_stream_t stream);
-
-/*
- * Workspace bytes oasis_sparse_decode_attn needs for these sizes on the
- * current device (the split depends on its SM count); 0 for invalid sizes.
- */
-size_t oasis_attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg);
+                             float *out, float *lse, int32_t *status, oasis_stream_t stream);
 
 #ifdef __cplusplus
 }

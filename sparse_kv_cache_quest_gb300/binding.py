@@ -23,7 +23,7 @@ STATUS_PLAN_RANGE, STATUS_SEQ_LEN, STATUS_TIMEOUT = 8, 16, 32
 
 EXPORTS = (
     "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks",
-    "oasis_select_topk_capped", "oasis_stage_blocks", "oasis_sparse_decode_attn", "oasis_attn_workspace_bytes",
+    "oasis_select_topk_capped", "oasis_stage_blocks", "oasis_sparse_decode_attn",
 )
 
 
@@ -51,8 +51,7 @@ _SIGS = {
     "oasis_score_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "oasis_select_topk_capped": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "oasis_stage_blocks": (_I, [_P, _I64, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P]),
-    "oasis_sparse_decode_attn": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, ctypes.c_size_t, _P, _P]),
-    "oasis_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "oasis_sparse_decode_attn": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
 }
 
 
@@ -134,20 +133,8 @@ def oasis_stage_blocks(host_kv, host_seg_stride_bytes, host_nb, plan, plan_count
         _ptr(pool), slots_per_seg, _ptr(status), _stream(stream)))
 
 
-def oasis_sparse_decode_attn(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws,
-                             ws_bytes, status=None, stream=None):
+def oasis_sparse_decode_attn(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse=None,
+                             status=None, stream=None):
     return _check("oasis_sparse_decode_attn", load().oasis_sparse_decode_attn(
         _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
-        _ptr(out), _ptr(lse), _ptr(ws), int(ws_bytes), _ptr(status), _stream(stream)))
-
-
-def oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg) -> int:
-    return int(load().oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg))
-
-
-def attn_workspace(B, Hkv, G, D, slots_per_seg, device="cuda") -> torch.Tensor:
-    """A device buffer large enough for oasis_sparse_decode_attn on these sizes."""
-    n = oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg)
-    if n == 0:
-        raise OasisError("oasis_attn_workspace_bytes", EINVAL, "invalid sizes")
-    return torch.empty(n, dtype=torch.uint8, device=device)
+        _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))

@@ -132,31 +132,18 @@ int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int h
                                            D, pool, slots_per_seg, status, stream));
 }
 
-namespace {
-bool attn_args_ok(int B, int Hkv, int G, int D, int slots_per_seg) {
-  if (!d_ok(D) || !segs_ok(B, Hkv) || G < 1 || G > 16 || slots_per_seg < 1 || slots_per_seg > 4096) return false;
-  return static_cast<int64_t>(B) * Hkv * slots_per_seg * 32 <= 0x7FFFFFFF;  // pool rows
-}
-}  // namespace
-
-size_t oasis_attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg) {
-  if (!attn_args_ok(B, Hkv, G, D, slots_per_seg)) return 0;
-  return oasis::attn_workspace_bytes(B, Hkv, G, D, slots_per_seg);
-}
-
 int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
                              const int32_t *seq_len, int B, int Hkv, int G, int D, float scale, float *out,
-                             float *lse, void *ws, size_t ws_bytes, int32_t *status, oasis_stream_t stream) {
-  if (!q || !pool || !table || !seq_len || !out || !ws) return OASIS_EINVAL;
-  if (!attn_args_ok(B, Hkv, G, D, slots_per_seg)) return OASIS_EINVAL;
-  if (!aligned16(q) || !aligned16(pool) || !aligned4(table) || !aligned4(seq_len) || !aligned4(out) ||
-      !aligned16(ws))
+                             float *lse, int32_t *status, oasis_stream_t stream) {
+  if (!q || !pool || !table || !seq_len || !out) return OASIS_EINVAL;
+  if (!d_ok(D) || !segs_ok(B, Hkv) || G < 1 || G > 16 || slots_per_seg < 1 || slots_per_seg > 4096)
+    return OASIS_EINVAL;
+  if (static_cast<int64_t>(B) * Hkv * slots_per_seg * 32 > 0x7FFFFFFF) return OASIS_EINVAL;  // pool rows
+  if (!aligned16(q) || !aligned16(pool) || !aligned4(table) || !aligned4(seq_len) || !aligned4(out))
     return OASIS_EINVAL;
   if ((lse && !aligned4(lse)) || (status && !aligned4(status))) return OASIS_EINVAL;
-  const size_t need = oasis::attn_workspace_bytes(B, Hkv, G, D, slots_per_seg);
-  if (need == 0 || ws_bytes < need) return OASIS_EINVAL;
   return finish(oasis::launch_sparse_decode_attn(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out,
-                                                 lse, ws, ws_bytes, status, stream));
+                                                 lse, status, stream));
 }
 
 }  // extern "C"

@@ -21,13 +21,9 @@
 // of at most `qseg` segments whose query operands it holds in shared memory;
 // its warps take the units of a phase round-robin.
 //
-// Data path.  Each warp streams the 8-dim chunks of its units (a chunk of a
-// 64-block unit is 1 KiB of kmin and 1 KiB of kmax, contiguous in the
-// chunk-major layout [S][D/8][Nb][8]) through a private ring of kNS stages
-// with 1-D bulk async copies (cp.async.bulk + mbarrier), across unit
-// boundaries; a stage is refilled as soon as its data is in registers.  Every
-// mbarrier wait is bounded and reports OASIS_STATUS_TIMEOUT instead of hanging.
-// Inner loop.  Per dim it widens kmin/kmax to fp32 and
+// Inner loop.  Lane b streams its block's 16-byte kmin/kmax chunks (8 dims of
+// the chunk-major layout [S][D/8][Nb][8], so a warp reads 512 contiguous bytes
+// per load) with kPF chunks in flight.  Per dim it widens kmin/kmax to fp32 and
 // runs two packed fp32x2 FMAs (fma.rn.f32x2) per pair of queries and block:
 // the query operands sit in shared memory as {qn_j, qn_j+1, qp_j, qp_j+1}, one
 // broadcast 16-byte load per pair and dim feeding 2*NB packed FMAs.  Queries are padded to NQP by repeating the
@@ -42,40 +38,36 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kNB = 2;               // blocks per lane
-constexpr int kUnit = 32 * kNB;      // blocks per warp unit
-constexpr int kNS = 4;               // ring stages per warp (one 8-dim chunk of a unit each)
-constexpr int kStage = 2 * kUnit * 16;  // kmin then kmax: 64 blocks x 16 bytes each
-constexpr uint32_t kWaitTries = 1u << 22;
-constexpr size_t kQBudget = 40 * 1024;  // query operands of the segments of one phase
+
+// Blocks per lane: two while the accumulators fit (each broadcast query load
+// then feeds four packed FMAs instead of two), else one.
+template <int NQP>
+constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
+template <int NQP>
+constexpr int min_ctas() { return 2; }
+template <int NQP>
+constexpr size_t smem_budget() { return 100 * 1024; }
+template <int NQP>
+constexpr int prefetch() { return 2; }  // chunks in flight per lane and block
 
 // CH = D / 8 chunks of 8 dims (8 for D = 64, 16 for D = 128).
 template <int NQP, int CH>
-__global__ void __launch_bounds__(kThreads, NQP <= 24 ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
     k_score(const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax, int Nb_max,
             const uint16_t *__restrict__ qdraft, int S, int Hkv, int G, int Nd, const int32_t *__restrict__ seq_len,
             int W, float *__restrict__ scores, int32_t *status, int units_per_seg, int qseg) {
   constexpr int D = CH * 8;
   constexpr int per_seg_q = D * (NQP / 2);
-  extern __shared__ __align__(16) unsigned char smraw[];
-  unsigned char *rings = smraw;                                           // [kWarps][kNS][kStage]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smraw + kWarps * kNS * kStage);  // [kWarps][kNS]
-  float4 *qsm = reinterpret_cast<float4 *>(bars + kWarps * kNS);        // [qseg][D][NQP/2]
+  constexpr int kPF = prefetch<NQP>();
+  constexpr int NB = blocks_per_lane<NQP>();
+  constexpr int kUnit = 32 * NB;  // blocks per warp unit
+  extern __shared__ float4 qsm[];  // [qseg][D][NQP/2] {qn_j, qn_j+1, qp_j, qp_j+1}
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
   const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
   if (u0 >= u1) return;
   const int Nq = G * Nd, Hq = Hkv * G;
   const int s_last = static_cast<int>((u1 - 1) / units_per_seg);
-  unsigned char *ring = rings + warp * kNS * kStage;
-  uint64_t *wbar = bars + warp * kNS;
-  if (lane == 0) {
-    for (int i = 0; i < kNS; ++i) mbar_init(&wbar[i], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  uint32_t phase_bits = 0;  // parity of the next completion of each stage (bit per stage)
-  bool timed_out = false;
 
   for (int s_lo = static_cast<int>(u0 / units_per_seg); s_lo <= s_last; s_lo += qseg) {
     const int s_hi = min(s_last + 1, s_lo + qseg);  // segments [s_lo, s_hi) in this phase
@@ -97,69 +89,58 @@ __global__ void __launch_bounds__(kThreads, NQP <= 24 ? 2 : 1)
     }
     __syncthreads();
 
-    // this warp's units of the phase: pu0 + warp + j * kWarps; items (j, chunk) in order
     const int64_t pu0 = std::max(u0, static_cast<int64_t>(s_lo) * units_per_seg);
     const int64_t pu1 = std::min(u1, static_cast<int64_t>(s_hi) * units_per_seg);
-    const int nunits = pu1 > pu0 + warp ? static_cast<int>((pu1 - pu0 - warp + kWarps - 1) / kWarps) : 0;
-    const int nitems = nunits * CH;
-    auto issue = [&](int i) {  // lane 0: bulk-copy item i into stage i % kNS
-      const int64_t u = pu0 + warp + static_cast<int64_t>(i / CH) * kWarps;
-      const int c = i % CH;
-      const int s = static_cast<int>(u / units_per_seg);
-      const int base = static_cast<int>(u % units_per_seg) * kUnit;
-      const uint32_t bytes = static_cast<uint32_t>(min(kUnit, Nb_max - base)) * 16u;
-      const int64_t off = ((static_cast<int64_t>(s) * CH + c) * Nb_max + base) * 8;
-      unsigned char *dst = ring + (i % kNS) * kStage;
-      mbar_arrive_expect_tx(&wbar[i % kNS], 2 * bytes);
-      bulk_g2s(dst, kmin + off, bytes, &wbar[i % kNS]);
-      bulk_g2s(dst + kUnit * 16, kmax + off, bytes, &wbar[i % kNS]);
-    };
-    if (lane == 0 && !timed_out)
-      for (int i = 0; i < kNS && i < nitems; ++i) issue(i);
-
-    // after a timed-out wait the warp skips its remaining work but still meets
-    // every CTA barrier of the later phases
-    unsigned long long acc[kNB][NQP / 2];
-    for (int j = 0; j < nunits && !timed_out; ++j) {
-      const int64_t u = pu0 + warp + static_cast<int64_t>(j) * kWarps;
+    for (int64_t u = pu0 + warp; u < pu1; u += kWarps) {
       const int s = static_cast<int>(u / units_per_seg);
       const int base = static_cast<int>(u % units_per_seg) * kUnit;
       const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status,
                              lane == 0 && base == 0 && (s % Hkv) == 0);
       const int nc = ceil_div(L, kBlockTokens) - W;
-      const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
+      if (base >= nc) continue;  // warp-uniform
+      int bl[NB];
 #pragma unroll
-      for (int i = 0; i < kNB; ++i)
+      for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, nc - 1);
+      const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
+      const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
+      const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
+
+      unsigned long long acc[NB][NQP / 2];
+#pragma unroll
+      for (int i = 0; i < NB; ++i)
 #pragma unroll
         for (int jp = 0; jp < NQP / 2; ++jp) acc[i][jp] = 0ull;  // (+0, +0)
-#pragma unroll 1
-      for (int c = 0; c < CH; ++c) {
-        const int it = j * CH + c, stg = it % kNS;
-        const bool ok = mbar_wait_bounded(&wbar[stg], (phase_bits >> stg) & 1u, kWaitTries);
-        phase_bits ^= 1u << stg;
-        if (__any_sync(0xFFFFFFFFu, !ok)) {
-          timed_out = true;
-          break;
-        }
-        const uint4 *st4 = reinterpret_cast<const uint4 *>(ring + stg * kStage);
-        uint4 mn[kNB], mx[kNB];
+      uint4 bmn[kPF][NB], bmx[kPF][NB];
 #pragma unroll
-        for (int i = 0; i < kNB; ++i) {
-          mn[i] = st4[lane + 32 * i];
-          mx[i] = st4[kUnit + lane + 32 * i];
+      for (int p = 0; p < kPF; ++p)
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
+          bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
         }
-        __syncwarp();  // the stage is in registers: refill it at once
-        if (lane == 0 && it + kNS < nitems) {
-          fence_proxy_async_smem();
-          issue(it + kNS);
+      // unrolled by kPF only (ring indices stay compile-time constants): the fully
+      // unrolled body overflows the instruction cache
+#pragma unroll 1
+      for (int c0 = 0; c0 < CH; c0 += kPF)
+#pragma unroll
+      for (int cc = 0; cc < kPF; ++cc) {
+        const int c = c0 + cc;
+        uint4 mn[NB], mx[NB];
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          mn[i] = bmn[cc][i];
+          mx[i] = bmx[cc][i];
+          if (c + kPF < CH) {
+            bmn[cc][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+            bmx[cc][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+          }
         }
-        if (base >= nc) continue;  // empty unit (warp-uniform): loaded, not scored
         const float4 *qrow = qbase + (c * 8) * (NQP / 2);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          unsigned long long kn2[kNB], kx2[kNB];
+          unsigned long long kn2[NB], kx2[NB];
 #pragma unroll
-          for (int i = 0; i < kNB; ++i) {
+          for (int i = 0; i < NB; ++i) {
             const uint32_t wn = e < 2 ? mn[i].x : e < 4 ? mn[i].y : e < 6 ? mn[i].z : mn[i].w;
             const uint32_t wx = e < 2 ? mx[i].x : e < 4 ? mx[i].y : e < 6 ? mx[i].z : mx[i].w;
             const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
@@ -172,16 +153,15 @@ __global__ void __launch_bounds__(kThreads, NQP <= 24 ? 2 : 1)
             const float4 qv = qrow[e * (NQP / 2) + jp];
             const unsigned long long qn2 = pack2(qv.x, qv.y), qp2 = pack2(qv.z, qv.w);
 #pragma unroll
-            for (int i = 0; i < kNB; ++i) {
+            for (int i = 0; i < NB; ++i) {
               acc[i][jp] = fma2(qn2, kn2[i], acc[i][jp]);
               acc[i][jp] = fma2(qp2, kx2[i], acc[i][jp]);
             }
           }
         }
       }
-      if (timed_out || base >= nc) continue;  // (the j loop ends after a timeout)
 #pragma unroll
-      for (int i = 0; i < kNB; ++i) {
+      for (int i = 0; i < NB; ++i) {
         float best = -FLT_MAX;
 #pragma unroll
         for (int jp = 0; jp < NQP / 2; ++jp) {
@@ -194,7 +174,6 @@ __global__ void __launch_bounds__(kThreads, NQP <= 24 ? 2 : 1)
       }
     }
   }
-  if (timed_out && lane == 0) report(status, OASIS_STATUS_TIMEOUT);
 }
 
 template <int NQP, int CH>
@@ -204,11 +183,12 @@ cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max
   constexpr int D = CH * 8;
   const int S = B * Hkv;
   const int ncand = std::max(1, Nb_max - W);
+  constexpr int kUnit = 32 * blocks_per_lane<NQP>();
   const int units_per_seg = (ncand + kUnit - 1) / kUnit;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
   const size_t per_seg = sizeof(float4) * static_cast<size_t>(D) * (NQP / 2);
-  const int qseg = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, kQBudget / per_seg)));
-  const size_t smem = static_cast<size_t>(kWarps) * kNS * (kStage + sizeof(uint64_t)) + per_seg * qseg;
+  const int qseg = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, smem_budget<NQP>() / per_seg)));
+  const size_t smem = per_seg * qseg;
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score<NQP, CH>), kThreads, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;

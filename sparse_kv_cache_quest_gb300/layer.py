@@ -68,8 +68,6 @@ class DecodeLayer:
         self.pool = torch.zeros((sh.S, sh.slots, 2, BLOCK, sh.D), dtype=torch.bfloat16, device=dev)
         self.out = torch.zeros((sh.B, sh.Hq, sh.D), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((sh.B, sh.Hq), dtype=torch.float32, device=dev)
-        with torch.cuda.device(dev):
-            self.ws = ob.attn_workspace(sh.B, sh.Hkv, sh.G, sh.D, sh.slots, device=dev)
         self.scale = 1.0 / math.sqrt(sh.D)
 
     # -- individual steps ---------------------------------------------------
@@ -103,7 +101,7 @@ class DecodeLayer:
     def attend(self, q, seq_len, stream=None):
         sh = self.shape
         ob.oasis_sparse_decode_attn(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D,
-                                    self.scale, self.out, self.lse, self.ws, self.ws.numel(), self.status, stream)
+                                    self.scale, self.out, self.lse, self.status, stream)
 
     def swap_tables(self):
         self.table, self.table_next = self.table_next, self.table

@@ -76,9 +76,6 @@ def test_select_validation(lib):
 def test_stage_and_attention_validation(lib):
     _einval(okv.oasis_stage_blocks, P, 8, 4, P, P, 2, 1, 1, 128, P, 8, P, 0)        # stride % 16
     _einval(okv.oasis_stage_blocks, P, 16, 0, P, P, 2, 1, 1, 128, P, 8, P, 0)       # host_nb
-    f = okv.oasis_sparse_decode_attn
-    _einval(f, P, P, P, 8, P, 1, 1, 0, 128, 0.1, P, None, P, 1 << 20, None, 0)        # G
-    _einval(f, P, P, P, 0, P, 1, 1, 4, 128, 0.1, P, None, P, 1 << 20, None, 0)        # slots
-    _einval(f, P + 8, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, P, 1 << 20, None, 0)    # q align
-    _einval(f, P, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, None, 1 << 20, None, 0)     # no workspace
-    assert okv.oasis_attn_workspace_bytes(1, 1, 0, 128, 8) == 0                      # invalid sizes
+    _einval(okv.oasis_sparse_decode_attn, P, P, P, 8, P, 1, 1, 0, 128, 0.1, P, None, None, 0)  # G
+    _einval(okv.oasis_sparse_decode_attn, P, P, P, 0, P, 1, 1, 4, 128, 0.1, P, None, None, 0)  # slots
+    _einval(okv.oasis_sparse_decode_attn, P + 8, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, None, 0)  # q align

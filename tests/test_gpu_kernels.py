@@ -316,9 +316,8 @@ def test_attention_within_tolerance(D, G, slots):
     out = torch.full((B, Hkv * G, D), 9.0, dtype=torch.float32, device=DEV)
     lse = torch.zeros((B, Hkv * G), dtype=torch.float32, device=DEV)
     scale = default_scale(D)
-    ws = okv.attn_workspace(B, Hkv, G, D, slots)
     okv.oasis_sparse_decode_attn(_dev_bf16(q), _dev_bf16(pool), torch.from_numpy(tables).to(DEV), slots,
-                                 torch.from_numpy(lens).to(DEV), B, Hkv, G, D, scale, out, lse, ws, ws.numel(), None)
+                                 torch.from_numpy(lens).to(DEV), B, Hkv, G, D, scale, out, lse, None)
     torch.cuda.synchronize()
     go, gl = out.cpu().numpy(), lse.cpu().numpy()
     for s in range(S):
