@@ -214,6 +214,26 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- multi-rank host logic
+
+def max_over_ranks(x, device=None):
+    """The largest of the ranks' values of x (x itself without a process group).
+    Each rank times its own replica; the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step, ms_per_step, world):
+    """Whole-job throughput: every rank moves its own step's bytes in the
+    (max-over-ranks) step time."""
+    return bytes_per_rank_step * world / (ms_per_step / 1e3) / 1e9
+
+
 # --------------------------------------------------------------------------- GPU side
 
 def _gpu_prior(w, lay, tiles, sl, q):
@@ -317,11 +337,7 @@ def run_ours(args):
     torch.cuda.nvtx.range_pop()
     barrier()
     clk = clocks.stop() if clocks else None
-    ms = e0.elapsed_time(e1) / layer_steps                  # per layer-step
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / layer_steps, dev)          # per layer-step, slowest rank
     st = torch.stack([lay.status for lay in insts]).max().item()
     assert st == 0, okv.strerror(int(st))
 
@@ -354,7 +370,7 @@ def run_ours(args):
         torch.cuda.nvtx.range_pop()
 
     per_layer = w.headline_bytes_per_layer()
-    value = per_layer * world / (ms / 1e3) / 1e9
+    value = job_gbs(per_layer, ms, world)
     peak, peak_kind = _peaks()
     score_bytes = w.summary_bytes_per_layer()
     attn_bytes = w.kv_bytes_per_layer() + w.out_bytes_per_layer()
@@ -431,12 +447,8 @@ def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time
     if world > 1:
         dist.barrier()
     reps = max(1, min(200, -(-args.steps // R)))
-    ms = time_replays(g.replay, reps) / R
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": w.headline_bytes_per_layer() * world / (ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+    ms = max_over_ranks(time_replays(g.replay, reps) / R, dev)
+    return {"value": job_gbs(w.headline_bytes_per_layer(), ms, world), "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": g.h2d_bytes // R, "d2h_bytes_per_step": g.d2h_bytes // R,
             "how": "DecodeStepGraph(host_io=True).replay(): per layer-step H2D of its inputs, the step, "
                    "D2H of its results"}

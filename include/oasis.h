@@ -132,8 +132,10 @@ int oasis_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_strid
  *               q_d * (q_d >= 0 ? kmax_d : kmin_d)
  * (each term is an exact fp32 product of two bf16 values, so the result is
  * reproducible bit for bit).
- * EINVAL: a NULL or misaligned pointer, D not 64 or 128, G not in [1, 16],
- * Nd < 1, G*Nd > 64, B or Hkv < 1, W < 0, Nb_max < 1.  status may be NULL.
+ * EINVAL: a NULL or misaligned pointer (kmin, kmax and qdraft need 16-byte
+ * alignment, seq_len, scores and status 4-byte), D not 64 or 128, G not in
+ * [1, 16], Nd < 1, G*Nd > 64, B or Hkv < 1, W < 0, Nb_max < 1.  status may be
+ * NULL.
  */
 int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
                        int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,

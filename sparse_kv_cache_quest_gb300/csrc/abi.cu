@@ -101,7 +101,8 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
   if (!kmin || !kmax || !qdraft || !seq_len || !scores) return OASIS_EINVAL;
   if (!d_ok(D) || !segs_ok(B, Hkv) || Nb_max < 1 || W < 0) return OASIS_EINVAL;
   if (G < 1 || G > 16 || Nd < 1 || G * Nd > 64) return OASIS_EINVAL;
-  if (!aligned16(kmin) || !aligned16(kmax) || !aligned4(seq_len) || !aligned4(scores)) return OASIS_EINVAL;
+  if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(qdraft) || !aligned4(seq_len) || !aligned4(scores))
+    return OASIS_EINVAL;
   if (status && !aligned4(status)) return OASIS_EINVAL;
   return finish(oasis::launch_score_blocks(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores,
                                            status, stream));

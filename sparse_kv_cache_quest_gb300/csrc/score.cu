@@ -44,7 +44,7 @@ constexpr int kWarps = kThreads / 32;
 template <int NQP>
 constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
 template <int NQP>
-constexpr int min_ctas() { return 2; }
+constexpr int min_ctas() { return NQP <= 12 ? 2 : 1; }
 template <int NQP>
 constexpr size_t smem_budget() { return 100 * 1024; }
 template <int NQP>
@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
   constexpr int kPF = prefetch<NQP>();
   constexpr int NB = blocks_per_lane<NQP>();
   constexpr int kUnit = 32 * NB;  // blocks per warp unit
+  constexpr int kFill = 2;        // raw query loads in flight per thread while filling qsm
   extern __shared__ float4 qsm[];  // [qseg][D][NQP/2] {qn_j, qn_j+1, qp_j, qp_j+1}
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
@@ -69,109 +70,146 @@ __global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
   const int Nq = G * Nd, Hq = Hkv * G;
   const int s_last = static_cast<int>((u1 - 1) / units_per_seg);
 
+  // State of the warp's current unit.  Its first kPF chunks and its sequence
+  // length are requested as soon as the unit is known; the block rows are
+  // clamped to the summary capacity (always inside the arrays), so the loads
+  // do not wait for the length.  Rows at or past nc are never written.
+  int s = 0, base = 0, Lraw = 0;
+  int bl[NB];
+  const uint4 *pmn = nullptr, *pmx = nullptr;
+  uint4 bmn[kPF][NB], bmx[kPF][NB];
+  auto start_unit = [&](int64_t u) {
+    s = static_cast<int>(u / units_per_seg);
+    base = static_cast<int>(u % units_per_seg) * kUnit;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, Nb_max - 1);
+    pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
+    pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
+#pragma unroll
+    for (int p = 0; p < kPF; ++p)
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
+        bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
+      }
+    Lraw = __ldg(seq_len + s / Hkv);
+  };
+
   for (int s_lo = static_cast<int>(u0 / units_per_seg); s_lo <= s_last; s_lo += qseg) {
     const int s_hi = min(s_last + 1, s_lo + qseg);  // segments [s_lo, s_hi) in this phase
-    __syncthreads();                                // the previous phase is done with qsm
-    for (int idx = tid; idx < (s_hi - s_lo) * per_seg_q; idx += kThreads) {
-      const int sl = idx / per_seg_q, rem = idx % per_seg_q;
-      const int d = rem / (NQP / 2), jp = rem % (NQP / 2);
-      const int s = s_lo + sl, bseq = s / Hkv, h = s % Hkv;
-      float qv[2];
+    const int64_t pu0 = std::max(u0, static_cast<int64_t>(s_lo) * units_per_seg);
+    const int64_t pu1 = std::min(u1, static_cast<int64_t>(s_hi) * units_per_seg);
+    int64_t u = pu0 + warp;
+    __syncthreads();  // the previous phase is done with qsm
+    if (u < pu1) start_unit(u);
+
+    // Query operands of the phase's segments: 16-byte loads of 8 dims of one
+    // (padded) query each, kFill in flight per thread, then split into the
+    // {qn, qn', qp, qp'} layout.  Item order (segment, chunk, query) keeps a
+    // warp's stores spread over the banks.
+    const int n_items = (s_hi - s_lo) * CH * NQP;
+    for (int i0 = 0; i0 < n_items; i0 += kFill * kThreads) {
+      uint4 raw[kFill];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int j = min(2 * jp + t, Nq - 1);
-        const int jd = j / G, g = j % G;
-        const uint16_t raw = qdraft[((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + d];
-        qv[t] = __uint_as_float(static_cast<uint32_t>(raw) << 16);
+      for (int k = 0; k < kFill; ++k) {
+        const int idx = i0 + k * kThreads + tid;
+        if (idx < n_items) {
+          const int sl = idx / (CH * NQP), rem = idx % (CH * NQP), c = rem / NQP;
+          const int j = min(rem % NQP, Nq - 1), jd = j / G, g = j % G;
+          const int sq = s_lo + sl, bseq = sq / Hkv, h = sq % Hkv;
+          raw[k] = __ldg(reinterpret_cast<const uint4 *>(
+              qdraft + ((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + c * 8));
+        }
       }
-      const bool p0 = qv[0] >= 0.0f, p1 = qv[1] >= 0.0f;
-      qsm[idx] = make_float4(p0 ? 0.0f : qv[0], p1 ? 0.0f : qv[1], p0 ? qv[0] : 0.0f, p1 ? qv[1] : 0.0f);
+#pragma unroll
+      for (int k = 0; k < kFill; ++k) {
+        const int idx = i0 + k * kThreads + tid;
+        if (idx < n_items) {
+          const int sl = idx / (CH * NQP), rem = idx % (CH * NQP), c = rem / NQP, j = rem % NQP;
+          float *dst = reinterpret_cast<float *>(qsm + sl * per_seg_q + (c * 8) * (NQP / 2) + (j >> 1)) + (j & 1);
+          const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float v = (e & 1) ? bf16_hi(w4[e >> 1]) : bf16_lo(w4[e >> 1]);
+            const bool pos = v >= 0.0f;
+            dst[e * (NQP / 2) * 4] = pos ? 0.0f : v;      // qn
+            dst[e * (NQP / 2) * 4 + 2] = pos ? v : 0.0f;  // qp
+          }
+        }
+      }
     }
     __syncthreads();
 
-    const int64_t pu0 = std::max(u0, static_cast<int64_t>(s_lo) * units_per_seg);
-    const int64_t pu1 = std::min(u1, static_cast<int64_t>(s_hi) * units_per_seg);
-    for (int64_t u = pu0 + warp; u < pu1; u += kWarps) {
-      const int s = static_cast<int>(u / units_per_seg);
-      const int base = static_cast<int>(u % units_per_seg) * kUnit;
-      const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status,
-                             lane == 0 && base == 0 && (s % Hkv) == 0);
+    for (; u < pu1; u += kWarps) {
+      int L = Lraw;
+      if (L < 0 || L > Nb_max * kBlockTokens) {
+        if (lane == 0 && base == 0 && (s % Hkv) == 0) report(status, OASIS_STATUS_SEQ_LEN);
+        L = L < 0 ? 0 : Nb_max * kBlockTokens;
+      }
       const int nc = ceil_div(L, kBlockTokens) - W;
-      if (base >= nc) continue;  // warp-uniform
-      int bl[NB];
+      if (base < nc) {  // warp-uniform
+        const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
+        unsigned long long acc[NB][NQP / 2];
 #pragma unroll
-      for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, nc - 1);
-      const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
-      const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
-      const float4 *qbase = qsm + (s - s_lo) * per_seg_q;
-
-      unsigned long long acc[NB][NQP / 2];
+        for (int i = 0; i < NB; ++i)
 #pragma unroll
-      for (int i = 0; i < NB; ++i)
-#pragma unroll
-        for (int jp = 0; jp < NQP / 2; ++jp) acc[i][jp] = 0ull;  // (+0, +0)
-      uint4 bmn[kPF][NB], bmx[kPF][NB];
-#pragma unroll
-      for (int p = 0; p < kPF; ++p)
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
-          bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
-        }
-      // unrolled by kPF only (ring indices stay compile-time constants): the fully
-      // unrolled body overflows the instruction cache
+          for (int jp = 0; jp < NQP / 2; ++jp) acc[i][jp] = 0ull;  // (+0, +0)
+        // unrolled by kPF only (ring indices stay compile-time constants): the fully
+        // unrolled body overflows the instruction cache
 #pragma unroll 1
-      for (int c0 = 0; c0 < CH; c0 += kPF)
+        for (int c0 = 0; c0 < CH; c0 += kPF)
 #pragma unroll
-      for (int cc = 0; cc < kPF; ++cc) {
-        const int c = c0 + cc;
-        uint4 mn[NB], mx[NB];
-#pragma unroll
-        for (int i = 0; i < NB; ++i) {
-          mn[i] = bmn[cc][i];
-          mx[i] = bmx[cc][i];
-          if (c + kPF < CH) {
-            bmn[cc][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
-            bmx[cc][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
-          }
-        }
-        const float4 *qrow = qbase + (c * 8) * (NQP / 2);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          unsigned long long kn2[NB], kx2[NB];
-#pragma unroll
-          for (int i = 0; i < NB; ++i) {
-            const uint32_t wn = e < 2 ? mn[i].x : e < 4 ? mn[i].y : e < 6 ? mn[i].z : mn[i].w;
-            const uint32_t wx = e < 2 ? mx[i].x : e < 4 ? mx[i].y : e < 6 ? mx[i].z : mx[i].w;
-            const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
-            const float fx = (e & 1) ? bf16_hi(wx) : bf16_lo(wx);
-            kn2[i] = pack2(fn, fn);
-            kx2[i] = pack2(fx, fx);
-          }
-#pragma unroll
-          for (int jp = 0; jp < NQP / 2; ++jp) {
-            const float4 qv = qrow[e * (NQP / 2) + jp];
-            const unsigned long long qn2 = pack2(qv.x, qv.y), qp2 = pack2(qv.z, qv.w);
+          for (int cc = 0; cc < kPF; ++cc) {
+            const int c = c0 + cc;
+            uint4 mn[NB], mx[NB];
 #pragma unroll
             for (int i = 0; i < NB; ++i) {
-              acc[i][jp] = fma2(qn2, kn2[i], acc[i][jp]);
-              acc[i][jp] = fma2(qp2, kx2[i], acc[i][jp]);
+              mn[i] = bmn[cc][i];
+              mx[i] = bmx[cc][i];
+              if (c + kPF < CH) {
+                bmn[cc][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+                bmx[cc][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+              }
+            }
+            const float4 *qrow = qbase + (c * 8) * (NQP / 2);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              unsigned long long kn2[NB], kx2[NB];
+#pragma unroll
+              for (int i = 0; i < NB; ++i) {
+                const uint32_t wn = e < 2 ? mn[i].x : e < 4 ? mn[i].y : e < 6 ? mn[i].z : mn[i].w;
+                const uint32_t wx = e < 2 ? mx[i].x : e < 4 ? mx[i].y : e < 6 ? mx[i].z : mx[i].w;
+                const float fn = (e & 1) ? bf16_hi(wn) : bf16_lo(wn);
+                const float fx = (e & 1) ? bf16_hi(wx) : bf16_lo(wx);
+                kn2[i] = pack2(fn, fn);
+                kx2[i] = pack2(fx, fx);
+              }
+#pragma unroll
+              for (int jp = 0; jp < NQP / 2; ++jp) {
+                const float4 qv = qrow[e * (NQP / 2) + jp];
+                const unsigned long long qn2 = pack2(qv.x, qv.y), qp2 = pack2(qv.z, qv.w);
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+                  acc[i][jp] = fma2(qn2, kn2[i], acc[i][jp]);
+                  acc[i][jp] = fma2(qp2, kx2[i], acc[i][jp]);
+                }
+              }
             }
           }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+          float best = -FLT_MAX;
+#pragma unroll
+          for (int jp = 0; jp < NQP / 2; ++jp) {
+            float a0, a1;
+            unpack2(acc[i][jp], a0, a1);
+            best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
+          }
+          const int b = base + lane + 32 * i;
+          if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
         }
       }
-#pragma unroll
-      for (int i = 0; i < NB; ++i) {
-        float best = -FLT_MAX;
-#pragma unroll
-        for (int jp = 0; jp < NQP / 2; ++jp) {
-          float a0, a1;
-          unpack2(acc[i][jp], a0, a1);
-          best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
-        }
-        const int b = base + lane + 32 * i;
-        if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
-      }
+      if (u + kWarps < pu1) start_unit(u + kWarps);
     }
   }
 }

@@ -63,6 +63,7 @@ def test_score_validation(lib):
     _einval(f, P, P, 16, P, 1, 1, 16, 5, 128, P, 0, P, None, 0)          # G*Nd > 64
     _einval(f, P, P, 16, P, 1, 1, 4, 1, 128, P, -1, P, None, 0)          # W < 0
     _einval(f, P, P, 0, P, 1, 1, 4, 1, 128, P, 0, P, None, 0)            # Nb_max
+    _einval(f, P, P, 16, P + 8, 1, 1, 4, 1, 128, P, 0, P, None, 0)       # qdraft not 16-byte aligned
 
 
 def test_select_validation(lib):
