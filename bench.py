@@ -415,7 +415,7 @@ def _traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the kernel's current source (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic_qwen3-8b-layer.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:

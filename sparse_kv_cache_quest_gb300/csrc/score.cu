@@ -36,7 +36,7 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 224;  // 7 warps: two CTAs cover 14 of the 16 warp slots 128 registers allow
 constexpr int kWarps = kThreads / 32;
 
 // Blocks per lane: two while the accumulators fit (each broadcast query load
@@ -225,13 +225,18 @@ cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max
   const int units_per_seg = (ncand + kUnit - 1) / kUnit;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
   const size_t per_seg = sizeof(float4) * static_cast<size_t>(D) * (NQP / 2);
-  const int qseg = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, smem_budget<NQP>() / per_seg)));
-  const size_t smem = per_seg * qseg;
+  const int qseg_max = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, smem_budget<NQP>() / per_seg)));
   int sms = 0, per_sm = 0;
-  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score<NQP, CH>), kThreads, smem, &sms, &per_sm);
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score<NQP, CH>), kThreads, per_seg * qseg_max,
+                                  &sms, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(std::min<int64_t>(want, U));  // every CTA gets >= 1 unit
+  // segments a CTA's unit range can touch: shared memory for just those (a small
+  // footprint leaves room for the kernels running beside this one)
+  const int64_t per_cta = (U + grid - 1) / grid;
+  const int qseg = static_cast<int>(std::min<int64_t>(qseg_max, (per_cta + units_per_seg - 1) / units_per_seg + 1));
+  const size_t smem = per_seg * qseg;
   k_score<NQP, CH><<<grid, kThreads, smem, st>>>(kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W, scores,
                                                   status, units_per_seg, qseg);
   return cudaGetLastError();

@@ -6,48 +6,55 @@
 //
 // The host copy of the full cache is pinned, mapped host memory that the GPU
 // reads directly (zero-copy): on a Grace-Blackwell node the loads travel over
-// NVLink-C2C, elsewhere over PCIe.  One CTA per plan entry copies one tile
-// (64*D bytes) with 16-byte loads, four in flight per thread before the
-// stores, so the link sees many outstanding requests.
+// NVLink-C2C, elsewhere over PCIe.  The copy is bound by that link, not by the
+// SMs, so the kernel is kept small: a few CTAs whose warps walk the plan
+// entries (segment-major) with a stride, one tile per warp at a time, all of
+// the tile's 16-byte loads issued before its stores.  That keeps about a
+// megabyte in flight, several times what the link needs to stay busy, while
+// occupying only kCtas SMs, so the kernels that run beside it on other streams
+// keep the rest of the machine.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCtas = 16;
+constexpr int kMaxPerLane = 16;  // 16-byte loads per lane for one tile at D = 128
 
 __global__ void __launch_bounds__(kThreads) k_stage(const unsigned char *__restrict__ host, int64_t seg_stride,
                                                     int host_nb, const oasis_xfer_t *__restrict__ plan,
-                                                    const int32_t *__restrict__ plan_count, int cap, int D,
+                                                    const int32_t *__restrict__ plan_count, int cap, int S, int D,
                                                     uint16_t *__restrict__ pool, int slots, int32_t *status) {
-  const int i = blockIdx.x, s = blockIdx.y;
-  int cnt = plan_count[s];
-  if (cnt < 0 || cnt > cap) {
-    if (threadIdx.x == 0 && i == 0) report(status, OASIS_STATUS_PLAN_RANGE);
-    cnt = cnt < 0 ? 0 : cap;
-  }
-  if (i >= cnt) return;
-  const oasis_xfer_t e = plan[static_cast<int64_t>(s) * cap + i];
-  if (e.src_block < 0 || e.src_block >= host_nb || e.dst_slot < 0 || e.dst_slot >= slots) {
-    if (threadIdx.x == 0) report(status, OASIS_STATUS_PLAN_RANGE);
-    return;
-  }
-  const int64_t tile_bytes = 64LL * D;
-  const uint4 *src = reinterpret_cast<const uint4 *>(host + s * seg_stride + e.src_block * tile_bytes);
-  uint4 *dst = reinterpret_cast<uint4 *>(pool + (static_cast<int64_t>(s) * slots + e.dst_slot) * 32 * D);
-  const int n16 = static_cast<int>(tile_bytes / 16);
-  for (int base = 0; base < n16; base += 4 * kThreads) {
-    uint4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int idx = base + u * kThreads + threadIdx.x;
-      if (idx < n16) v[u] = src[idx];
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * kWarps;
+  const int n16 = 4 * D;  // 16-byte words per tile (64*D bytes)
+  const int64_t entries = static_cast<int64_t>(S) * cap;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); e < entries; e += nw) {
+    const int s = static_cast<int>(e / cap), i = static_cast<int>(e % cap);
+    int cnt = plan_count[s];
+    if (cnt < 0 || cnt > cap) {
+      if (lane == 0 && i == 0) report(status, OASIS_STATUS_PLAN_RANGE);
+      cnt = cnt < 0 ? 0 : cap;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int idx = base + u * kThreads + threadIdx.x;
-      if (idx < n16) dst[idx] = v[u];
+    if (i >= cnt) continue;  // warp-uniform
+    const oasis_xfer_t x = plan[e];
+    if (x.src_block < 0 || x.src_block >= host_nb || x.dst_slot < 0 || x.dst_slot >= slots) {
+      if (lane == 0) report(status, OASIS_STATUS_PLAN_RANGE);
+      continue;
     }
+    const uint4 *src = reinterpret_cast<const uint4 *>(host + s * seg_stride + x.src_block * (64LL * D));
+    uint4 *dst = reinterpret_cast<uint4 *>(pool + (static_cast<int64_t>(s) * slots + x.dst_slot) * 32 * D);
+    uint4 v[kMaxPerLane];
+#pragma unroll
+    for (int u = 0; u < kMaxPerLane; ++u)
+      if (u * 32 + lane < n16) v[u] = src[u * 32 + lane];
+#pragma unroll
+    for (int u = 0; u < kMaxPerLane; ++u)
+      if (u * 32 + lane < n16) dst[u * 32 + lane] = v[u];
   }
 }
 
@@ -57,9 +64,11 @@ cudaError_t launch_stage_blocks(const void *host_kv, int64_t host_seg_stride_byt
                                 const oasis_xfer_t *plan, const int32_t *plan_count, int cap, int B, int Hkv,
                                 int D, uint16_t *pool, int slots_per_seg, int32_t *status, cudaStream_t st) {
   if (cap == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(cap), static_cast<unsigned>(B * Hkv));
+  const int S = B * Hkv;
+  const int64_t warps_needed = static_cast<int64_t>(S) * cap;
+  const int grid = static_cast<int>(std::min<int64_t>(kCtas, (warps_needed + kWarps - 1) / kWarps));
   k_stage<<<grid, kThreads, 0, st>>>(static_cast<const unsigned char *>(host_kv), host_seg_stride_bytes, host_nb,
-                                      plan, plan_count, cap, D, pool, slots_per_seg, status);
+                                      plan, plan_count, cap, S, D, pool, slots_per_seg, status);
   return cudaGetLastError();
 }
 
