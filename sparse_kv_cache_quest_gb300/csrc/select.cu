@@ -31,6 +31,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr size_t kStaticSmemBound = 4096;  // >= the kernel's static shared memory (3 KiB of histograms + scalars)
 
 __device__ __forceinline__ uint32_t score_key(float f, bool &nan) {
   uint32_t u = __float_as_uint(f);
@@ -86,6 +87,8 @@ struct SelScalars {
   int warp_tot[kWarps];
 };
 
+static_assert(sizeof(SelScalars) + 3 * 256 * sizeof(uint32_t) <= kStaticSmemBound, "static shared memory bound");
+
 __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ scores, int Nb_max,
                                                      const int32_t *__restrict__ seq_len, int Hkv, int K, int W,
                                                      int cap, const int32_t *table_in, int32_t *table_out,
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
                                                      int32_t *status) {
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ SelScalars sc;
-  __shared__ uint32_t hist[256];
+  __shared__ __align__(16) uint32_t hist[3][256];  // pass p counts into hist[p % 3], clears hist[(p + 1) % 3]
 
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
     sc.err = 0;
     sc.nN = sc.nE = sc.nF = sc.nEmpty = 0;
   }
+  for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
   bool nan = false;
   const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
   for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
@@ -161,9 +165,10 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
   } else {
     uint32_t prefix = 0u, pmask = 0u;
     int remaining = K;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += kThreads) hist[i] = 0u;
-      __syncthreads();
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      uint32_t *h = hist[pass % 3];
+      for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0u;
       for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
         const int b = b0 + lane;
         int dig = -1;
@@ -172,41 +177,49 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
           if ((key & pmask) == prefix) dig = static_cast<int>((key >> shift) & 0xFFu);
         }
         const unsigned grp = __match_any_sync(0xFFFFFFFFu, dig);
-        if (dig >= 0 && lane == __ffs(grp) - 1) atomicAdd(&hist[dig], static_cast<uint32_t>(__popc(grp)));
+        if (dig >= 0 && lane == __ffs(grp) - 1) atomicAdd(&h[dig], static_cast<uint32_t>(__popc(grp)));
       }
+      // The only barrier of the pass: the counts are complete, the next buffer is
+      // clear, and every warp has finished reading the buffer cleared next pass.
       __syncthreads();
-      if (warp == 0) {
-        // lane l owns bins 255-8l down to 248-8l (descending digit order)
-        uint32_t c[8];
-        uint32_t sum = 0;
+      // Every warp finds the digit of the remaining-th largest key on its own.
+      // Lane l owns bins 255-8l down to 248-8l (descending digit order).
+      // (two 16-byte loads per lane: consecutive lanes read consecutive 16-byte
+      // chunks, so every warp's reads are free of bank conflicts)
+      const uint4 lo4 = reinterpret_cast<const uint4 *>(h)[62 - 2 * lane];  // bins 248-8l .. 251-8l
+      const uint4 hi4 = reinterpret_cast<const uint4 *>(h)[63 - 2 * lane];  // bins 252-8l .. 255-8l
+      const uint32_t c[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+      uint32_t sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sum += c[q];
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t before = incl - sum;
+      uint32_t digit = 0u;
+      int rem = 0;
+      const bool mine = before < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl;
+      if (mine) {
+        uint32_t cum = before;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          c[q] = hist[255 - 8 * lane - q];
-          sum += c[q];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t before = incl - sum;
-        if (before < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl) {
-          uint32_t cum = before;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (cum < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= cum + c[q]) {
-              sc.digit = static_cast<uint32_t>(255 - 8 * lane - q);
-              sc.remaining = remaining - static_cast<int>(cum);
-            }
-            cum += c[q];
+          if (cum < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= cum + c[q]) {
+            digit = static_cast<uint32_t>(255 - 8 * lane - q);
+            rem = remaining - static_cast<int>(cum);
           }
+          cum += c[q];
         }
       }
-      __syncthreads();
-      prefix |= sc.digit << shift;
+      const unsigned holders = __ballot_sync(0xFFFFFFFFu, mine);  // exactly one lane holds it
+      const int src = holders ? __ffs(holders) - 1 : 0;
+      digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+      rem = __shfl_sync(0xFFFFFFFFu, rem, src);
+      prefix |= digit << shift;
       pmask |= 0xFFu << shift;
-      remaining = sc.remaining;
+      remaining = rem;
     }
     const uint32_t tau = prefix;
     const int need = remaining;  // keys equal to tau to take, lowest block id first
@@ -250,40 +263,54 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
   const int nEvict = max(0, nA - nEmpty);
   const int nFill = nA - nEvict;
 
-  // 5. A = the nA best of N; freed slots = first nFill empty slots + the nEvict worst of E
-  for (int i = tid; i < nN; i += kThreads) {
+  // 5. A = the nA best of N; freed slots = first nFill empty slots + the nEvict worst of E.
+  // Every rank is a count over a list of at most K entries: one warp per entry,
+  // its lanes splitting the list, a ballot-popcount per 32 entries.
+  for (int i = warp; i < nN; i += kWarps) {
     const uint64_t ci = listN[i];
     int r = 0;
-    for (int j = 0; j < nN; ++j) r += listN[j] > ci;
-    rankN[i] = r;
+    for (int j0 = 0; j0 < nN; j0 += 32) {
+      const int j = j0 + lane;
+      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && listN[j] > ci));
+    }
+    if (lane == 0) rankN[i] = r;
   }
-  for (int i = tid; i < nE; i += kThreads) {
+  for (int i = warp; i < nE; i += kWarps) {
     const uint64_t ci = listE[i];
     int r = 0;
-    for (int j = 0; j < nE; ++j) r += listE[j] < ci;
-    if (r < nEvict) {
+    for (int j0 = 0; j0 < nE; j0 += 32) {
+      const int j = j0 + lane;
+      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nE && listE[j] < ci));
+    }
+    if (lane == 0 && r < nEvict) {
       const int f = atomicAdd(&sc.nF, 1);
       if (f < cap) fList[f] = slotE[i];
     }
   }
-  for (int i = tid; i < K; i += kThreads) {
-    if (tin[i] == -1) {
-      int r = 0;
-      for (int j = 0; j < i; ++j) r += tin[j] == -1;
-      if (r < nFill) {
+  if (nFill > 0) {
+    for (int i = warp; i < K; i += kWarps) {
+      if (tin[i] != -1) continue;  // warp-uniform
+      int r = 0;                   // empty slots before slot i
+      for (int j0 = 0; j0 < i; j0 += 32) {
+        const int j = j0 + lane;
+        r += __popc(__ballot_sync(0xFFFFFFFFu, j < i && tin[j] == -1));
+      }
+      if (lane == 0 && r < nFill) {
         const int f = atomicAdd(&sc.nF, 1);
         if (f < cap) fList[f] = i;
       }
     }
   }
   __syncthreads();
-  for (int i = tid; i < nN; i += kThreads) {
-    if (rankN[i] < nA) {
-      const int b = composite_block(listN[i]);
-      int r = 0;
-      for (int j = 0; j < nN; ++j) r += rankN[j] < nA && composite_block(listN[j]) < b;
-      if (r < cap) aSorted[r] = b;
+  for (int i = warp; i < nN; i += kWarps) {
+    if (rankN[i] >= nA) continue;  // warp-uniform
+    const int b = composite_block(listN[i]);
+    int r = 0;
+    for (int j0 = 0; j0 < nN; j0 += 32) {
+      const int j = j0 + lane;
+      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && rankN[j] < nA && composite_block(listN[j]) < b));
     }
+    if (lane == 0 && r < cap) aSorted[r] = b;
   }
   for (int i = tid; i < nA; i += kThreads) {
     const int sl = fList[i];
@@ -320,7 +347,9 @@ cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                                       oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st) {
   const size_t smem = select_smem_bytes(Nb_max, K, W, cap);
-  if (smem > 48 * 1024) {
+  // static (histograms, scalars) + dynamic shared memory may pass the 48 KiB
+  // default before the dynamic part alone does
+  if (smem + kStaticSmemBound > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
