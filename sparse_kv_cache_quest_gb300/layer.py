@@ -224,11 +224,12 @@ class DecodeStepGraph:
     shared); with host_io=True the graph first copies every layer's inputs from
     pinned host staging tensors and ends by copying every layer's results
     (out, lse, new table, plan, plan counts) back to pinned host memory.  Tables do not
-    advance (the new tables stay in ``table_next``).
+    advance (the new tables stay in ``table_next``).  n_bg: background streams,
+    taken by the layers in turn.
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
-                 new_block: Optional[int] = None, host_io: bool = False):
+                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2):
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
@@ -242,7 +243,12 @@ class DecodeStepGraph:
         self.host_in = [[t.cpu().pin_memory() for t in x] for x in ins] if host_io else None
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
-        fg, bg, sel, xf = (torch.cuda.Stream(dev) for _ in range(4))
+        fg, sel, xf = (torch.cuda.Stream(dev) for _ in range(3))
+        # two background streams taken by alternate layers: the background of
+        # layer l+1 needs only the foreground to have passed layer l, so it may
+        # start while layer l's scoring still runs, which hides each scoring
+        # kernel's start-up and tail behind its neighbour
+        bgs = [torch.cuda.Stream(dev) for _ in range(n_bg)]
         stage_args = (host_kv, host_seg_stride_bytes, host_nb)
 
         def body(cur):
@@ -252,10 +258,11 @@ class DecodeStepGraph:
                         d.copy_(h, non_blocking=True)
             start = torch.cuda.Event()
             start.record(cur)
-            for st in (fg, bg, sel, xf):
+            for st in (fg, sel, xf, *bgs):
                 st.wait_event(start)
             prev_fg = None
             for i, lay in enumerate(layers):
+                bg = bgs[i % len(bgs)]
                 if prev_fg is not None:
                     bg.wait_event(prev_fg)                     # the forward pass has reached layer i
                 if new_keys is not None:
@@ -274,7 +281,7 @@ class DecodeStepGraph:
                 xf.wait_event(e_sel)
                 xf.wait_event(e_fg)
                 lay.stage(*stage_args, stream=xf)
-            for st in (fg, bg, sel, xf):
+            for st in (fg, sel, xf, *bgs):
                 e = torch.cuda.Event()
                 e.record(st)
                 cur.wait_event(e)
