@@ -434,9 +434,9 @@ def _traffic(kernel):
 def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time_replays):
     """Same metric through the public call with host buffers: every decode step
     is one DecodeStepGraph(host_io=True) replay that copies each layer's inputs
-    (queries, drafts, newest block's keys) from pinned host memory, runs the R
-    layers and copies each layer's results (outputs, lse, new table, plan,
-    counts) back to pinned host memory."""
+    (queries, drafts, newest block's keys) from pinned host memory before the
+    layer's work and each layer's results (outputs, lse, new table, plan,
+    counts) back to pinned host memory once they exist."""
     import torch
     import torch.distributed as dist
 
@@ -452,8 +452,9 @@ def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time
     ms = max_over_ranks(time_replays(g.replay, reps) / R, dev)
     return {"value": job_gbs(w.headline_bytes_per_layer(), ms, world), "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": g.h2d_bytes // R, "d2h_bytes_per_step": g.d2h_bytes // R,
-            "how": "DecodeStepGraph(host_io=True).replay(): per layer-step H2D of its inputs, the step, "
-                   "D2H of its results"}
+            "how": "DecodeStepGraph(host_io=True).replay(): every layer-step copies its inputs from pinned host "
+                   "memory (one copy) before its work and its results back after it, on copy streams that "
+                   "overlap the other layers' kernels"}
 
 
 def main():

@@ -209,6 +209,23 @@ class StepGraph:
         self.graph.replay()
 
 
+def _arena(tensors, dev):
+    """One uint8 device buffer holding copies of ``tensors`` (each at a 256-byte
+    aligned offset) and typed views of it in the tensors' shapes."""
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    arena = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = []
+    for t, o in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        v = arena[o:o + n].view(t.dtype).view(t.shape)
+        v.copy_(t.detach())
+        views.append(v)
+    return arena, views
+
+
 class DecodeStepGraph:
     """One decode step through several layers as one CUDA graph, pipelined
     across layers as in the asynchronous prefetch pipeline of the OasisKV paper
@@ -220,10 +237,13 @@ class DecodeStepGraph:
     slots that attention reads) and must end before the next step, where the
     graph ends.
 
-    Each layer gets static input buffers (q, qdraft, new_keys; seq_len is
-    shared); with host_io=True the graph first copies every layer's inputs from
-    pinned host staging tensors and ends by copying every layer's results
-    (out, lse, new table, plan, plan counts) back to pinned host memory.  Tables do not
+    Each layer gets static input buffers (q, qdraft, new_keys, packed in one
+    device buffer per layer; seq_len is shared); with host_io=True the graph
+    copies each layer's inputs from a pinned host buffer (``host_in[i]``, one
+    copy) before that layer's work and each layer's results (out, lse, new
+    table, plan, plan counts) back to pinned host memory (``host_out[i]``) once
+    they exist, on two copy streams, so the copies overlap other layers'
+    kernels.  Tables do not
     advance (the new tables stay in ``table_next``).  n_bg: background streams,
     taken by the layers in turn.
     """
@@ -233,17 +253,27 @@ class DecodeStepGraph:
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
-        self.q = [q.detach().to(dev).clone() for _ in layers]
-        self.qdraft = [qdraft.detach().to(dev).clone() for _ in layers]
-        self.new_keys = [new_keys.detach().to(dev).contiguous().clone() if new_keys is not None else None
-                         for _ in layers]
-        ins = [[self.q[i], self.qdraft[i]] + ([self.new_keys[i]] if new_keys is not None else [])
-               for i in range(len(layers))]
+        # per layer, one contiguous device buffer holds that layer's inputs (q, qdraft,
+        # new keys), so host I/O moves them with a single copy
+        srcs = [q, qdraft] + ([new_keys] if new_keys is not None else [])
+        self.in_dev, self.in_host, views = [], [], []
+        for _ in layers:
+            arena, v = _arena(srcs, dev)
+            self.in_dev.append(arena)
+            views.append(v)
+            if host_io:
+                self.in_host.append(arena.cpu().pin_memory())
+        self.q = [v[0] for v in views]
+        self.qdraft = [v[1] for v in views]
+        self.new_keys = [v[2] if new_keys is not None else None for v in views]
         outs = [[l.out, l.lse, l.table_next, l.plan, l.plan_count] for l in layers]
-        self.host_in = [[t.cpu().pin_memory() for t in x] for x in ins] if host_io else None
+        self.host_in = self.in_host if host_io else None
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
         fg, sel, xf = (torch.cuda.Stream(dev) for _ in range(3))
+        # host I/O on copy streams of its own, per layer, so that the copies of one
+        # layer overlap the kernels of the others
+        h2d, d2h = (torch.cuda.Stream(dev) for _ in range(2)) if host_io else (None, None)
         # two background streams taken by alternate layers: the background of
         # layer l+1 needs only the foreground to have passed layer l, so it may
         # start while layer l's scoring still runs, which hides each scoring
@@ -251,18 +281,23 @@ class DecodeStepGraph:
         bgs = [torch.cuda.Stream(dev) for _ in range(n_bg)]
         stage_args = (host_kv, host_seg_stride_bytes, host_nb)
 
+        copy_streams = (h2d, d2h) if host_io else ()
+
         def body(cur):
-            if host_io:
-                for i in range(len(layers)):
-                    for d, h in zip(ins[i], self.host_in[i]):
-                        d.copy_(h, non_blocking=True)
             start = torch.cuda.Event()
             start.record(cur)
-            for st in (fg, sel, xf, *bgs):
+            for st in (fg, sel, xf, *bgs, *copy_streams):
                 st.wait_event(start)
             prev_fg = None
             for i, lay in enumerate(layers):
                 bg = bgs[i % len(bgs)]
+                if host_io:
+                    with torch.cuda.stream(h2d):
+                        self.in_dev[i].copy_(self.in_host[i], non_blocking=True)
+                    e_in = torch.cuda.Event()
+                    e_in.record(h2d)
+                    bg.wait_event(e_in)
+                    fg.wait_event(e_in)
                 if prev_fg is not None:
                     bg.wait_event(prev_fg)                     # the forward pass has reached layer i
                 if new_keys is not None:
@@ -281,14 +316,16 @@ class DecodeStepGraph:
                 xf.wait_event(e_sel)
                 xf.wait_event(e_fg)
                 lay.stage(*stage_args, stream=xf)
-            for st in (fg, sel, xf, *bgs):
+                if host_io:
+                    d2h.wait_event(e_sel)
+                    d2h.wait_event(e_fg)
+                    with torch.cuda.stream(d2h):
+                        for h, d in zip(self.host_out[i], outs[i]):
+                            h.copy_(d, non_blocking=True)
+            for st in (fg, sel, xf, *bgs, *copy_streams):
                 e = torch.cuda.Event()
                 e.record(st)
                 cur.wait_event(e)
-            if host_io:
-                for i in range(len(layers)):
-                    for h, d in zip(self.host_out[i], outs[i]):
-                        h.copy_(d, non_blocking=True)
 
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
@@ -299,7 +336,7 @@ class DecodeStepGraph:
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=side):
             body(side)
-        self.h2d_bytes = sum(t.numel() * t.element_size() for x in (self.host_in or []) for t in x)
+        self.h2d_bytes = sum(t.numel() for t in (self.host_in or []))
         self.d2h_bytes = sum(t.numel() * t.element_size() for x in (self.host_out or []) for t in x)
 
     def replay(self):
