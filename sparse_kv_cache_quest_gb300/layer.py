@@ -245,11 +245,12 @@ class DecodeStepGraph:
     they exist, on two copy streams, so the copies overlap other layers'
     kernels.  Tables do not
     advance (the new tables stay in ``table_next``).  n_bg: background streams,
-    taken by the layers in turn.
+    taken by the layers in turn; fg_priority: CUDA stream priority of the
+    foreground stream (lower is higher; 0 = default).
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
-                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2):
+                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2, fg_priority: int = 0):
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
@@ -270,7 +271,8 @@ class DecodeStepGraph:
         self.host_in = self.in_host if host_io else None
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
-        fg, sel, xf = (torch.cuda.Stream(dev) for _ in range(3))
+        fg = torch.cuda.Stream(dev, priority=fg_priority)
+        sel, xf = (torch.cuda.Stream(dev) for _ in range(2))
         # host I/O on copy streams of its own, per layer, so that the copies of one
         # layer overlap the kernels of the others
         h2d, d2h = (torch.cuda.Stream(dev) for _ in range(2)) if host_io else (None, None)
