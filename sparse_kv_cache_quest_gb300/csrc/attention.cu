@@ -417,20 +417,15 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   CL = std::min(CL, slots);
   while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // each warp's list fits
   if (CL > 8) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(CL);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(kThreads), smem, st);
+  cudaLaunchAttribute cl;
+  cl.id = cudaLaunchAttributeClusterDimension;
+  cl.val.clusterDim.x = static_cast<unsigned>(CL);
+  cl.val.clusterDim.y = 1;
+  cl.val.clusterDim.z = 1;
+  lc.add(cl);
   const float scale_log2 = scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&cfg, k_attn<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
+  return cudaLaunchKernelEx(&lc.cfg, k_attn<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
                             status);
 }
 

@@ -93,6 +93,35 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 }  // namespace oasis
 
+// Launch configuration carrying the priority of the launch stream as a launch
+// attribute, so that a stream capture records it in the graph's kernel node
+// (a priority set only on the capturing stream does not reach the graph).
+// Use in place: cfg.attrs points into this object.
+namespace oasis {
+struct LaunchCfg {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    int prio = 0;
+    if (cudaStreamGetPriority(st, &prio) != cudaSuccess) {
+      prio = 0;
+      (void)cudaGetLastError();
+    }
+    attr[0].id = cudaLaunchAttributePriority;
+    attr[0].val.priority = prio;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  LaunchCfg(const LaunchCfg &) = delete;
+  LaunchCfg &operator=(const LaunchCfg &) = delete;
+  void add(const cudaLaunchAttribute &a) { attr[cfg.numAttrs++] = a; }
+};
+}  // namespace oasis
+
 // Launchers implemented by the kernel translation units (host side).
 namespace oasis {
 cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm);

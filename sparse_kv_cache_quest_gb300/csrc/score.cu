@@ -43,8 +43,12 @@ constexpr int kWarps = kThreads / 32;
 // then feeds four packed FMAs instead of two), else one.
 template <int NQP>
 constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
+// Register cap: 128 keeps two 7-warp CTAs per SM (14 of the 16 warp slots the
+// register file allows at 128); the wide query groups take up to 255 with one CTA
+// per SM.  (A 112 cap, which would leave room beside two CTAs for an attention CTA
+// of another layer, spills and measured slower in the pipelined decode step.)
 template <int NQP>
-constexpr int min_ctas() { return NQP <= 12 ? 2 : 1; }
+constexpr int max_regs() { return NQP <= 12 ? 128 : 255; }
 template <int NQP>
 constexpr size_t smem_budget() { return 100 * 1024; }
 template <int NQP>
@@ -52,7 +56,7 @@ constexpr int prefetch() { return 2; }  // chunks in flight per lane and block
 
 // CH = D / 8 chunks of 8 dims (8 for D = 64, 16 for D = 128).
 template <int NQP, int CH>
-__global__ void __launch_bounds__(kThreads, min_ctas<NQP>())
+__global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
     k_score(const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax, int Nb_max,
             const uint16_t *__restrict__ qdraft, int S, int Hkv, int G, int Nd, const int32_t *__restrict__ seq_len,
             int W, float *__restrict__ scores, int32_t *status, int units_per_seg, int qseg) {
@@ -237,9 +241,9 @@ cudaError_t launch_nqp_ch(const uint16_t *kmin, const uint16_t *kmax, int Nb_max
   const int64_t per_cta = (U + grid - 1) / grid;
   const int qseg = static_cast<int>(std::min<int64_t>(qseg_max, (per_cta + units_per_seg - 1) / units_per_seg + 1));
   const size_t smem = per_seg * qseg;
-  k_score<NQP, CH><<<grid, kThreads, smem, st>>>(kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W, scores,
-                                                  status, units_per_seg, qseg);
-  return cudaGetLastError();
+  LaunchCfg lc(dim3(grid), dim3(kThreads), smem, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_score<NQP, CH>, kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W, scores,
+                            status, units_per_seg, qseg);
 }
 
 template <int NQP>

@@ -354,9 +354,9 @@ cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  k_select<<<B * Hkv, kThreads, smem, st>>>(scores, Nb_max, seq_len, Hkv, K, W, cap, table_in, table_out, plan,
-                                             plan_count, status);
-  return cudaGetLastError();
+  LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_select, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in, table_out, plan,
+                            plan_count, status);
 }
 
 }  // namespace oasis

@@ -67,9 +67,9 @@ cudaError_t launch_stage_blocks(const void *host_kv, int64_t host_seg_stride_byt
   const int S = B * Hkv;
   const int64_t warps_needed = static_cast<int64_t>(S) * cap;
   const int grid = static_cast<int>(std::min<int64_t>(kCtas, (warps_needed + kWarps - 1) / kWarps));
-  k_stage<<<grid, kThreads, 0, st>>>(static_cast<const unsigned char *>(host_kv), host_seg_stride_bytes, host_nb,
-                                      plan, plan_count, cap, S, D, pool, slots_per_seg, status);
-  return cudaGetLastError();
+  LaunchCfg lc(dim3(grid), dim3(kThreads), 0, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_stage, static_cast<const unsigned char *>(host_kv), host_seg_stride_bytes,
+                            host_nb, plan, plan_count, cap, S, D, pool, slots_per_seg, status);
 }
 
 }  // namespace oasis

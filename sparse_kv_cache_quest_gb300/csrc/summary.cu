@@ -85,10 +85,9 @@ cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t 
   const int threads = 256;
   const int64_t grid = (items + threads - 1) / threads;
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  k_build_summary<<<static_cast<unsigned>(grid), threads, 0, st>>>(k, seg_stride, blk_stride, tok_stride, Hkv, D,
-                                                                  seq_len, blk_begin, blk_count, S, kmin, kmax,
-                                                                  Nb_max, status);
-  return cudaGetLastError();
+  LaunchCfg lc(dim3(static_cast<unsigned>(grid)), dim3(threads), 0, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_build_summary, k, seg_stride, blk_stride, tok_stride, Hkv, D, seq_len,
+                            blk_begin, blk_count, S, kmin, kmax, Nb_max, status);
 }
 
 }  // namespace oasis
