@@ -112,7 +112,8 @@ def _to_chunk_major(x):  # [S][Nb][D] uint16 -> device [S][D/8][Nb][8]
 
 
 @pytest.mark.parametrize("D,G,Nd,W", [(128, 4, 3, 0), (64, 2, 1, 0), (128, 1, 1, 3), (128, 16, 4, 0),
-                                      (64, 3, 2, 2), (128, 16, 1, 0), (128, 5, 3, 1)])
+                                      (64, 3, 2, 2), (128, 16, 1, 0), (128, 5, 3, 1), (128, 8, 3, 0),
+                                      (128, 10, 4, 1), (64, 13, 1, 2), (64, 16, 4, 0)])
 def test_scores_bit_exact(D, G, Nd, W):
     rng = np.random.default_rng(100 + D + G * 7 + Nd)
     B, Hkv, Nb = 2, 2, 700
