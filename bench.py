@@ -54,6 +54,8 @@ def _args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--bg-streams", type=int, default=2, help="background streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
+    p.add_argument("--attn", choices=["cluster", "balanced"], default="cluster",
+                   help="attention split: per-head thread-block clusters, or SM-balanced with a workspace")
     return p.parse_args()
 
 
@@ -303,7 +305,7 @@ def run_ours(args):
     strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
     insts = []
     for i in range(R):
-        lay = okv.DecodeLayer(shape, device=dev)
+        lay = okv.DecodeLayer(shape, device=dev, balanced_attn=args.attn == "balanced")
         lay.build_summary(tiles, sl, 0, w.Nb, strides=strides)
         insts.append(lay)
     table0 = _gpu_prior(w, insts[0], tiles, sl, q).to(dev)
@@ -431,6 +433,7 @@ def run_ours(args):
                     "layers_per_decode_step": R,
                     "background_streams": args.bg_streams,
                     "foreground_priority": args.fg_priority,
+                    "attention_split": args.attn,
                     "step": "one pass of the whole path (summary update, scoring, capped selection, staging, "
                             "attention) over one layer; decode steps of R such layers run as one CUDA graph, "
                             "layer-pipelined (background of layer l overlaps the attention of later layers)",

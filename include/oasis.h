@@ -17,6 +17,8 @@
  *   oasis_select_topk_capped  top-K, capped admission, eviction, plan, table
  *   oasis_stage_blocks        host-resident KV tiles -> HBM slots (the plan)
  *   oasis_sparse_decode_attn  attention of the true query over the slots
+ *                             (oasis_sparse_decode_attn_ws: SM-balanced, with a
+ *                             caller workspace)
  *
  * Conventions shared by every entry point
  *   Memory.     The caller allocates and owns every buffer.  The library
@@ -207,6 +209,33 @@ int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int h
 int oasis_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
                              const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,
                              float *out, float *lse, int32_t *status, oasis_stream_t stream);
+
+/*
+ * The same attention with the work balanced over the SMs: all segments' slots
+ * form one range split evenly over the CTAs, so the SMs stream equal byte
+ * counts whatever the number of segments.  A segment whose slots are spread
+ * over several CTAs is merged by the CTA that finishes its part last, through
+ * partial results (running max, sum, output) and one arrival counter per
+ * segment kept in the caller's workspace (the same split-K merge as the
+ * cluster path, [XR] §4 Fig. 9 names only the attention, not its split).
+ * Results equal oasis_sparse_decode_attn's within rounding.
+ *
+ * ws:  device memory of at least oasis_attn_workspace_bytes(B, Hkv, G, D,
+ *      slots_per_seg) bytes, 16-byte aligned, ZERO-FILLED before its first
+ *      use.  It holds the partial results (scratch) and the per-segment
+ *      arrival counters; every call that completes leaves the counters at zero
+ *      again, so the workspace can be reused without clearing.  Calls that may
+ *      run at the same time (other streams) need workspaces of their own.
+ *      After a call that set OASIS_STATUS_TIMEOUT it must be zero-filled again.
+ * oasis_attn_workspace_bytes returns 0 for arguments the call would reject.
+ * EINVAL: as oasis_sparse_decode_attn, or ws NULL / misaligned, or ws_bytes
+ * smaller than the workspace size.
+ */
+size_t oasis_attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg);
+int oasis_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
+                                const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,
+                                float *out, float *lse, void *ws, size_t ws_bytes, int32_t *status,
+                                oasis_stream_t stream);
 
 #ifdef __cplusplus
 }

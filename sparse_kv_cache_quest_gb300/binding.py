@@ -24,6 +24,7 @@ STATUS_PLAN_RANGE, STATUS_SEQ_LEN, STATUS_TIMEOUT = 8, 16, 32
 EXPORTS = (
     "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks",
     "oasis_select_topk_capped", "oasis_stage_blocks", "oasis_sparse_decode_attn",
+    "oasis_attn_workspace_bytes", "oasis_sparse_decode_attn_ws",
 )
 
 
@@ -52,6 +53,9 @@ _SIGS = {
     "oasis_select_topk_capped": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "oasis_stage_blocks": (_I, [_P, _I64, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P]),
     "oasis_sparse_decode_attn": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "oasis_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "oasis_sparse_decode_attn_ws": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, ctypes.c_size_t, _P,
+                                         _P]),
 }
 
 
@@ -138,3 +142,23 @@ def oasis_sparse_decode_attn(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, 
     return _check("oasis_sparse_decode_attn", load().oasis_sparse_decode_attn(
         _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
         _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
+
+
+def oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg) -> int:
+    return int(load().oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg))
+
+
+def oasis_sparse_decode_attn_ws(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws,
+                                ws_bytes, status=None, stream=None):
+    return _check("oasis_sparse_decode_attn_ws", load().oasis_sparse_decode_attn_ws(
+        _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
+        _ptr(out), _ptr(lse), _ptr(ws), int(ws_bytes), _ptr(status), _stream(stream)))
+
+
+def attn_workspace(B, Hkv, G, D, slots_per_seg, device=None):
+    """A zero-filled device workspace for oasis_sparse_decode_attn_ws (uint8 tensor)."""
+    import torch
+    n = oasis_attn_workspace_bytes(B, Hkv, G, D, slots_per_seg)
+    if n == 0:
+        raise ValueError("oasis_attn_workspace_bytes rejected the arguments")
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")

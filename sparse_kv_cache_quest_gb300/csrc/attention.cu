@@ -30,6 +30,10 @@
 // Warps combine through shared memory (reusing the rings), then the CL CTAs of
 // the cluster combine through distributed shared memory into rank 0, which
 // writes out and lse.  No global scratch memory is used.
+//
+// k_attn_bal (further down) is the alternative split over all segments' slots
+// with a caller workspace; it measured slower than the cluster split on the
+// shapes benchmarked and is only used when a caller asks for it.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -103,6 +107,84 @@ struct Plan {
   static constexpr int kScratchBytes = 4 * (kCtaO + GQ * D);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
+
+// One 16-token slot tile in shared memory (swizzled as the tensor map writes it)
+// folded into a warp's online softmax state, on the tensor cores:
+//   S^T = K . Q^T, log2-domain online softmax over the tile's nv valid tokens,
+//   O^T += V^T . P^T with P^T split into bf16 hi + lo parts.
+template <int KS, int NT>
+__device__ __forceinline__ void attend_tile(uint32_t tile, int nv, const uint32_t (&qb)[NT][KS][2], float scale_log2,
+                                            float (&o)[NT][KS][4], float (&m)[NT][2], float (&l)[NT][2]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  // fragment addressing inside a swizzled tile: row r, 16-byte chunk j of the D-wide row
+  auto frag_addr = [](uint32_t tile, int r, int j) {
+    return tile + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4);
+  };
+  const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);  // K rows 0..15 for ldmatrix
+  const int khalf = lane >> 4;
+  const int vrow = 16 + (lane & 7) + 8 * (lane >> 4);   // V rows 16..31 for ldmatrix.trans
+  const int vhalf = (lane >> 3) & 1;
+
+  // ---- S^T = K . Q^T
+  float sacc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.0f;
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(frag_addr(tile, krow, 2 * ks + khalf), a);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mma16816(sacc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+  }
+  // ---- online softmax over the slot's tokens (rows g and g + 8), per query column
+  const bool v0 = g < nv, v1 = g + 8 < nv;
+  uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float p0[2], p1[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float x0 = v0 ? sacc[nt][j] * scale_log2 : -INFINITY;
+      const float x1 = v1 ? sacc[nt][2 + j] * scale_log2 : -INFINITY;
+      float mx = fmaxf(x0, x1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+      const float mn = fmaxf(m[nt][j], mx);
+      const float corr = exp2f(m[nt][j] - mn);
+      m[nt][j] = mn;
+      p0[j] = exp2f(x0 - mn);
+      p1[j] = exp2f(x1 - mn);
+      l[nt][j] = l[nt][j] * corr + p0[j] + p1[j];
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[nt][mt][j] *= corr;
+        o[nt][mt][2 + j] *= corr;
+      }
+    }
+    // P^T B-fragments: hi and lo bf16 parts, transposed 8x8 per token half
+    const uint32_t h0 = pack_bf16(p0[0], p0[1]), h1 = pack_bf16(p1[0], p1[1]);
+    const uint32_t l0 = pack_bf16(p0[0] - bf16_lo(h0), p0[1] - bf16_hi(h0));
+    const uint32_t l1 = pack_bf16(p1[0] - bf16_lo(h1), p1[1] - bf16_hi(h1));
+    bh[nt][0] = transpose8x8(h0);
+    bh[nt][1] = transpose8x8(h1);
+    bl[nt][0] = transpose8x8(l0);
+    bl[nt][1] = transpose8x8(l1);
+  }
+  // ---- O^T += V^T . P^T
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    uint32_t a[4];
+    ldsm_x4_t(frag_addr(tile, vrow, 2 * mt + vhalf), a);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma16816(o[nt][mt], a, bh[nt][0], bh[nt][1]);
+      mma16816(o[nt][mt], a, bl[nt][0], bl[nt][1]);
+    }
+  }
+}
 
 // KS = D / 16 (k-steps of the QK product and m-tiles of the PV product);
 // NT = query tiles of 8 heads (GQ = 8 * NT columns).
@@ -202,15 +284,6 @@ __global__ void __launch_bounds__(kThreads)
   int issued = min(kNST, count), consumed = 0;
   bool timed_out = false;
 
-  // fragment addressing inside a swizzled tile: row r, 16-byte chunk j of the D-wide row
-  auto frag_addr = [&](uint32_t tile, int r, int j) {
-    return tile + (j >> 3) * 4096 + r * 128 + (((j & 7) ^ (r & 7)) << 4);
-  };
-  const int krow = (lane & 7) + 8 * ((lane >> 3) & 1);  // K rows 0..15 for ldmatrix
-  const int khalf = lane >> 4;
-  const int vrow = 16 + (lane & 7) + 8 * (lane >> 4);   // V rows 16..31 for ldmatrix.trans
-  const int vhalf = (lane >> 3) & 1;
-
   for (int c = 0; c < count; ++c) {
     const int stg = c % kNST;
     const bool ok = mbar_wait_bounded(&bars[stg], static_cast<uint32_t>(c / kNST) & 1u, kWaitTries);
@@ -221,65 +294,7 @@ __global__ void __launch_bounds__(kThreads)
     const int nv = list[c] & 31;
     const uint32_t tile = ring + stg * P::kTile;
 
-    // ---- S^T = K . Q^T
-    float sacc[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.0f;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(frag_addr(tile, krow, 2 * ks + khalf), a);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816(sacc[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
-    }
-    // ---- online softmax over the slot's tokens (rows g and g + 8), per query column
-    const bool v0 = g < nv, v1 = g + 8 < nv;
-    uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float p0[2], p1[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float x0 = v0 ? sacc[nt][j] * scale_log2 : -INFINITY;
-        const float x1 = v1 ? sacc[nt][2 + j] * scale_log2 : -INFINITY;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-        const float mn = fmaxf(m[nt][j], mx);
-        const float corr = exp2f(m[nt][j] - mn);
-        m[nt][j] = mn;
-        p0[j] = exp2f(x0 - mn);
-        p1[j] = exp2f(x1 - mn);
-        l[nt][j] = l[nt][j] * corr + p0[j] + p1[j];
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[nt][mt][j] *= corr;
-          o[nt][mt][2 + j] *= corr;
-        }
-      }
-      // P^T B-fragments: hi and lo bf16 parts, transposed 8x8 per token half
-      const uint32_t h0 = pack_bf16(p0[0], p0[1]), h1 = pack_bf16(p1[0], p1[1]);
-      const uint32_t l0 = pack_bf16(p0[0] - bf16_lo(h0), p0[1] - bf16_hi(h0));
-      const uint32_t l1 = pack_bf16(p1[0] - bf16_lo(h1), p1[1] - bf16_hi(h1));
-      bh[nt][0] = transpose8x8(h0);
-      bh[nt][1] = transpose8x8(h1);
-      bl[nt][0] = transpose8x8(l0);
-      bl[nt][1] = transpose8x8(l1);
-    }
-    // ---- O^T += V^T . P^T
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a[4];
-      ldsm_x4_t(frag_addr(tile, vrow, 2 * mt + vhalf), a);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mma16816(o[nt][mt], a, bh[nt][0], bh[nt][1]);
-        mma16816(o[nt][mt], a, bl[nt][0], bl[nt][1]);
-      }
-    }
+    attend_tile<KS, NT>(tile, nv, qb, scale_log2, o, m, l);
     __syncwarp();
     ++consumed;
     if (c + kNST < count) {
@@ -372,6 +387,258 @@ __global__ void __launch_bounds__(kThreads)
   cluster.sync();
 }
 
+// ---- balanced split with a caller workspace --------------------------------
+// All segments' slots form one flat range of N = S * slots tiles; CTA c of P
+// takes [c*N/P, (c+1)*N/P), so every SM streams the same number of tiles
+// whatever the segment count.  A CTA walks the segments its range touches
+// ("pieces"), each as above (per-warp slot lists, 2-stage TMA rings, tensor-core
+// tile math, warp merge in shared memory).  A piece that is a whole segment is
+// written to out/lse directly.  A partial piece leaves (m, l, o) in the
+// workspace (its CTA's slot 0 for the first piece of its range, 1 for the
+// last), then the CTA counts itself in the segment's arrival counter; the CTA
+// that arrives last merges all pieces of the segment, writes out/lse and sets
+// the counter back to zero.  No CTA ever waits for another.
+__host__ __device__ __forceinline__ int64_t cta_of(int64_t x, int64_t N, int64_t P) { return ((x + 1) * P - 1) / N; }
+
+template <int KS, int NT>
+__global__ void __launch_bounds__(kThreads)
+    k_attn_bal(const __grid_constant__ CUtensorMap tmap, const uint16_t *__restrict__ q,
+               const int32_t *__restrict__ table, int slots, const int32_t *__restrict__ seq_len, int Hkv, int G,
+               float scale_log2, float *__restrict__ out, float *__restrict__ lse, int32_t *status,
+               float *__restrict__ part, int32_t *__restrict__ counter, int64_t N, int P) {
+  constexpr int D = 16 * KS;
+  constexpr int GQ = 8 * NT;
+  constexpr int kBoxes = D / 64;
+  using PL = Plan<D, GQ>;
+  extern __shared__ unsigned char sm_raw[];
+  __shared__ int s_merge;
+  const uint32_t raw_addr = smem_addr(sm_raw);
+  unsigned char *sm = sm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int Hq = Hkv * G;
+  const int part_floats = G * (D + 2);  // m[G], l[G], o[G][D]
+  const int64_t x0 = N * blockIdx.x / P, x1 = N * (blockIdx.x + 1) / P;
+  if (x0 >= x1) return;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + PL::kBars) + warp * kNST;
+  int32_t *list = reinterpret_cast<int32_t *>(sm + PL::kLists) + warp * kListMax;
+  const uint32_t ring = sbase + warp * kNST * PL::kTile;
+  if (lane == 0) {
+    for (int i = 0; i < kNST; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  uint32_t tc = 0;        // tiles this warp has issued and consumed so far (ring position, phase)
+  bool dead = false;      // a wait of this warp timed out: it stops streaming
+  const int seg_first = static_cast<int>(x0 / slots), seg_last = static_cast<int>((x1 - 1) / slots);
+
+  for (int s = seg_first; s <= seg_last; ++s) {
+    const int64_t seg_lo = static_cast<int64_t>(s) * slots;
+    const int a = static_cast<int>(std::max(x0, seg_lo) - seg_lo);
+    const int b = static_cast<int>(std::min(x1, seg_lo + slots) - seg_lo);  // slots [a, b) of segment s
+    const int bseq = s / Hkv, h = s % Hkv;
+    int L = seq_len[bseq];
+    if (L < 0) {
+      if (tid == 0 && a == 0 && h == 0) report(status, OASIS_STATUS_SEQ_LEN);
+      L = 0;
+    }
+    uint32_t qb[NT][KS][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int qi = nt * 8 + g;
+      const uint32_t *row =
+          reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bseq) * Hq + h * G + qi) * D);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qb[nt][ks][0] = qi < G ? row[(16 * ks + 2 * t) >> 1] : 0u;
+        qb[nt][ks][1] = qi < G ? row[(16 * ks + 8 + 2 * t) >> 1] : 0u;
+      }
+    }
+    float o[NT][KS][4];
+    float m[NT][2], l[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        m[nt][j] = -INFINITY;
+        l[nt][j] = 0.0f;
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[nt][mt][i] = 0.0f;
+    }
+    // this warp's non-empty slots of the piece, as (slot << 5 | valid tokens)
+    const int nk = (b - a) > warp ? (b - a - warp + kWarps - 1) / kWarps : 0;
+    const int32_t *trow = table + seg_lo;
+    int count = 0;
+    for (int base = 0; base < nk; base += 32) {
+      const int k = base + lane;
+      int nv = 0, slot = 0;
+      if (k < nk) {
+        slot = a + warp + kWarps * k;
+        const int blk = trow[slot];
+        const int64_t n = blk < 0 ? 0 : static_cast<int64_t>(L) - static_cast<int64_t>(kBlockTokens) * blk;
+        nv = n <= 0 ? 0 : (n >= kBlockTokens ? kBlockTokens : static_cast<int>(n));
+      }
+      const unsigned mk = __ballot_sync(0xFFFFFFFFu, nv > 0);
+      if (nv > 0) list[count + __popc(mk & ((1u << lane) - 1u))] = (slot << 5) | nv;
+      count += __popc(mk);
+    }
+    __syncwarp();
+    if (dead) count = 0;
+    const int row_base = s * slots;
+    auto issue = [&](int c) {
+      const int stg = static_cast<int>((tc + c) % kNST);
+      mbar_arrive_expect_tx(&bars[stg], PL::kTile);
+      const int y = (row_base + (list[c] >> 5)) * 32;
+#pragma unroll
+      for (int bx = 0; bx < kBoxes; ++bx)
+        tma_load_2d(ring + stg * PL::kTile + bx * 4096, &tmap, bx * 64, y, &bars[stg]);
+    };
+    if (lane == 0) {
+      fence_proxy_async_smem();  // the ring was last written as merge scratch
+      for (int c = 0; c < kNST && c < count; ++c) issue(c);
+    }
+    int issued = min(kNST, count), consumed = 0;
+    for (int c = 0; c < count; ++c) {
+      const uint32_t gi = tc + static_cast<uint32_t>(c);
+      const int stg = static_cast<int>(gi % kNST);
+      const bool ok = mbar_wait_bounded(&bars[stg], (gi / kNST) & 1u, kWaitTries);
+      if (__any_sync(0xFFFFFFFFu, !ok)) {
+        dead = true;
+        break;
+      }
+      attend_tile<KS, NT>(ring + stg * PL::kTile, list[c] & 31, qb, scale_log2, o, m, l);
+      __syncwarp();
+      ++consumed;
+      if (c + kNST < count) {
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          issue(c + kNST);
+        }
+        ++issued;
+      }
+    }
+    if (dead) {
+      if (lane == 0) report(status, OASIS_STATUS_TIMEOUT);
+      for (int c = consumed; c < issued; ++c) {
+        const uint32_t gi = tc + static_cast<uint32_t>(c);
+        mbar_wait_bounded(&bars[gi % kNST], (gi / kNST) & 1u, kWaitTries);
+      }
+    }
+    tc += static_cast<uint32_t>(dead ? issued : count);
+
+    // ---- warp totals, then the CTA's partial (m, l, o) of the piece in shared memory
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float v = l[nt][j];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        l[nt][j] = v;
+      }
+    __syncthreads();  // every warp is past its ring: the scratch may alias it
+    float *scratch = reinterpret_cast<float *>(sm);
+    float *wm = scratch + PL::kWarpM, *wl = scratch + PL::kWarpL, *wo = scratch + PL::kWarpO;
+    float *cm = scratch + PL::kCtaM, *cl = scratch + PL::kCtaL, *co = scratch + PL::kCtaO;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          wm[warp * GQ + nt * 8 + 2 * t + j] = m[nt][j];
+          wl[warp * GQ + nt * 8 + 2 * t + j] = l[nt][j];
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int qc = nt * 8 + 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
+          wo[(warp * GQ + qc) * D + dim] = o[nt][mt][i];
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+      const int qc = idx / D, d = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * GQ + qc]);
+      float acc = 0.0f, ls = 0.0f;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = exp2f(wm[w * GQ + qc] - M);
+          acc += f * wo[(w * GQ + qc) * D + d];
+          ls += f * wl[w * GQ + qc];
+        }
+      }
+      co[qc * D + d] = acc;
+      if (d == 0) {
+        cm[qc] = M;
+        cl[qc] = ls;
+      }
+    }
+    __syncthreads();
+
+    const int64_t c_first = cta_of(seg_lo, N, P), c_last = cta_of(seg_lo + slots - 1, N, P);
+    if (c_first == c_last) {  // the whole segment is this CTA's piece
+      for (int idx = tid; idx < G * D; idx += kThreads) {
+        const int qc = idx / D, d = idx % D;
+        const float ls = cl[qc];
+        const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
+        out[row * D + d] = ls > 0.0f ? co[idx] / ls : 0.0f;
+        if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (cm[qc] + log2f(ls)) * kLn2 : -INFINITY;
+      }
+    } else {
+      const int which = s == seg_first ? 0 : 1;
+      float *pp = part + (static_cast<int64_t>(blockIdx.x) * 2 + which) * part_floats;
+      for (int idx = tid; idx < G * D; idx += kThreads) pp[2 * G + idx] = co[(idx / D) * D + idx % D];
+      for (int qc = tid; qc < G; qc += kThreads) {
+        pp[qc] = cm[qc];
+        pp[G + qc] = cl[qc];
+      }
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int arrived = atomicAdd(&counter[s], 1);
+        s_merge = arrived == static_cast<int>(c_last - c_first);
+      }
+      __syncthreads();
+      if (s_merge) {
+        __threadfence();
+        for (int idx = tid; idx < G * D; idx += kThreads) {
+          const int qc = idx / D, d = idx % D;
+          float M = -INFINITY;
+          for (int64_t c = c_first; c <= c_last; ++c) {
+            const int sl = (N * c / P) / slots == s ? 0 : 1;
+            M = fmaxf(M, __ldcg(part + (c * 2 + sl) * part_floats + qc));
+          }
+          float acc = 0.0f, ls = 0.0f;
+          if (M > -INFINITY) {
+            for (int64_t c = c_first; c <= c_last; ++c) {
+              const int sl = (N * c / P) / slots == s ? 0 : 1;
+              const float *pc = part + (c * 2 + sl) * part_floats;
+              const float f = exp2f(__ldcg(pc + qc) - M);
+              acc += f * __ldcg(pc + 2 * G + idx);
+              ls += f * __ldcg(pc + G + qc);
+            }
+          }
+          const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
+          out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
+          if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+        }
+        if (tid == 0) counter[s] = 0;
+      }
+    }
+    __syncthreads();  // scratch and s_merge are reused by the next piece
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -429,6 +696,52 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
                             status);
 }
 
+// Grid of the balanced split: two CTAs per SM, at least enough CTAs that no
+// warp's list of a piece exceeds kListMax, never more CTAs than slot tiles
+// (so that every CTA owns at least one tile).
+int64_t bal_grid(int64_t N) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    sms = 1;
+  }
+  const int64_t per_cta = static_cast<int64_t>(kWarps) * kListMax;
+  const int64_t P = std::max<int64_t>(2 * static_cast<int64_t>(sms), (N + per_cta - 1) / per_cta);
+  return std::min(P, N);
+}
+
+template <int KS, int NT>
+cudaError_t launch_bal_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
+                         const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
+                         int32_t *status, float *part, int32_t *counter, cudaStream_t st) {
+  constexpr int D = 16 * KS;
+  using PL = Plan<D, 8 * NT>;
+  const int S = B * Hkv;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S) * slots * 32};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const size_t smem = PL::kEnd + 1024;
+  int sms = 0, per_sm = 0;
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn_bal<KS, NT>), kThreads, smem, &sms, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int64_t N = static_cast<int64_t>(S) * slots;
+  const int64_t P = bal_grid(N);
+  if (P > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  LaunchCfg lc(dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, st);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  return cudaLaunchKernelEx(&lc.cfg, k_attn_bal<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out,
+                            lse, status, part, counter, N, static_cast<int>(P));
+}
+
 }  // namespace
 
 cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table,
@@ -440,6 +753,37 @@ cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, c
   }
   if (G <= 8) return launch_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
   return launch_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+}
+
+size_t attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg) {
+  const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
+  const int64_t P = bal_grid(N);
+  const size_t parts = static_cast<size_t>(P) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  const size_t counters = static_cast<size_t>(B) * Hkv * sizeof(int32_t);
+  return (parts + 255) / 256 * 256 + counters;
+}
+
+cudaError_t launch_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool, const int32_t *table,
+                                         int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G, int D,
+                                         float scale, float *out, float *lse, void *ws, int32_t *status,
+                                         cudaStream_t st) {
+  const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
+  const int64_t P = bal_grid(N);
+  const size_t parts = static_cast<size_t>(P) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  float *part = static_cast<float *>(ws);
+  int32_t *counter = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + (parts + 255) / 256 * 256);
+  if (D == 128) {
+    if (G <= 8)
+      return launch_bal_t<8, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                                counter, st);
+    return launch_bal_t<8, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                              counter, st);
+  }
+  if (G <= 8)
+    return launch_bal_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                              counter, st);
+  return launch_bal_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                            counter, st);
 }
 
 }  // namespace oasis

@@ -51,9 +51,13 @@ class LayerShape:
 
 
 class DecodeLayer:
-    """Device buffers of one layer: summaries, scores, tables, plan, pool, outputs."""
+    """Device buffers of one layer: summaries, scores, tables, plan, pool, outputs.
 
-    def __init__(self, shape: LayerShape, device="cuda"):
+    balanced_attn: run the attention as the SM-balanced split with a workspace
+    of this layer's own (oasis_sparse_decode_attn_ws) instead of the per-head
+    cluster split (oasis_sparse_decode_attn)."""
+
+    def __init__(self, shape: LayerShape, device="cuda", balanced_attn: bool = False):
         self.shape = sh = shape
         dev = torch.device(device)
         self.device = dev
@@ -69,6 +73,7 @@ class DecodeLayer:
         self.out = torch.zeros((sh.B, sh.Hq, sh.D), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((sh.B, sh.Hq), dtype=torch.float32, device=dev)
         self.scale = 1.0 / math.sqrt(sh.D)
+        self.attn_ws = ob.attn_workspace(sh.B, sh.Hkv, sh.G, sh.D, sh.slots, device=dev) if balanced_attn else None
 
     # -- individual steps ---------------------------------------------------
     def build_summary(self, keys, seq_len, blk_begin=0, blk_count=None, strides=None, stream=None):
@@ -100,6 +105,11 @@ class DecodeLayer:
 
     def attend(self, q, seq_len, stream=None):
         sh = self.shape
+        if self.attn_ws is not None:
+            ob.oasis_sparse_decode_attn_ws(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D,
+                                           self.scale, self.out, self.lse, self.attn_ws, self.attn_ws.numel(),
+                                           self.status, stream)
+            return
         ob.oasis_sparse_decode_attn(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D,
                                     self.scale, self.out, self.lse, self.status, stream)
 

@@ -74,6 +74,17 @@ def test_select_validation(lib):
     _einval(f, P, 40000, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)             # Nb_max too large
 
 
+def test_attention_workspace_validation(lib):
+    assert okv.oasis_attn_workspace_bytes(2, 4, 4, 128, 128) > 0
+    assert okv.oasis_attn_workspace_bytes(2, 4, 4, 96, 128) == 0                    # D
+    assert okv.oasis_attn_workspace_bytes(2, 4, 17, 128, 128) == 0                  # G
+    f = okv.oasis_sparse_decode_attn_ws
+    n = okv.oasis_attn_workspace_bytes(1, 1, 4, 128, 8)
+    _einval(f, P, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, None, n, None, 0)      # NULL workspace
+    _einval(f, P, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, P, n - 1, None, 0)     # workspace too small
+    _einval(f, P, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, P + 8, n, None, 0)     # misaligned workspace
+
+
 def test_stage_and_attention_validation(lib):
     _einval(okv.oasis_stage_blocks, P, 8, 4, P, P, 2, 1, 1, 128, P, 8, P, 0)        # stride % 16
     _einval(okv.oasis_stage_blocks, P, 16, 0, P, P, 2, 1, 1, 128, P, 8, P, 0)       # host_nb

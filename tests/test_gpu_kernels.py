@@ -290,9 +290,10 @@ def test_stage_copies_exactly_the_plan():
 
 # ------------------------------------------------------------------ attention
 
+@pytest.mark.parametrize("ws", [False, True])
 @pytest.mark.parametrize("D,G,slots", [(128, 4, 128), (64, 2, 37), (128, 1, 5), (128, 8, 64), (128, 16, 128),
                                        (64, 5, 20), (128, 3, 1)])
-def test_attention_within_tolerance(D, G, slots):
+def test_attention_within_tolerance(D, G, slots, ws):
     rng = np.random.default_rng(D + G * 13 + slots)
     B, Hkv, Nb = 2, 3, 300
     S = B * Hkv
@@ -317,9 +318,25 @@ def test_attention_within_tolerance(D, G, slots):
     out = torch.full((B, Hkv * G, D), 9.0, dtype=torch.float32, device=DEV)
     lse = torch.zeros((B, Hkv * G), dtype=torch.float32, device=DEV)
     scale = default_scale(D)
-    okv.oasis_sparse_decode_attn(_dev_bf16(q), _dev_bf16(pool), torch.from_numpy(tables).to(DEV), slots,
-                                 torch.from_numpy(lens).to(DEV), B, Hkv, G, D, scale, out, lse, None)
+    args = (_dev_bf16(q), _dev_bf16(pool), torch.from_numpy(tables).to(DEV), slots, torch.from_numpy(lens).to(DEV),
+            B, Hkv, G, D, scale, out, lse)
+    st = _status()
+    if ws:
+        # the balanced split: two calls in a row on one workspace (its counters must come back to zero)
+        work = okv.attn_workspace(B, Hkv, G, D, slots, device=DEV)
+        okv.oasis_sparse_decode_attn_ws(*args, work, work.numel(), st)
+        torch.cuda.synchronize()
+        first = out.clone()
+        out.fill_(9.0)
+        okv.oasis_sparse_decode_attn_ws(*args, work, work.numel(), st)
+        torch.cuda.synchronize()
+        assert torch.equal(out, first)
+        counters = work[-4 * S:].view(torch.int32)
+        assert int(counters.abs().sum()) == 0
+    else:
+        okv.oasis_sparse_decode_attn(*args, st)
     torch.cuda.synchronize()
+    assert st.item() == 0
     go, gl = out.cpu().numpy(), lse.cpu().numpy()
     for s in range(S):
         b, h = divmod(s, Hkv)
