@@ -24,7 +24,7 @@ STATUS_PLAN_RANGE, STATUS_SEQ_LEN, STATUS_TIMEOUT = 8, 16, 32
 EXPORTS = (
     "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks",
     "oasis_select_topk_capped", "oasis_stage_blocks", "oasis_sparse_decode_attn",
-    "oasis_attn_workspace_bytes", "oasis_sparse_decode_attn_ws",
+    "oasis_attn_workspace_bytes", "oasis_sparse_decode_attn_ws", "oasis_sparse_decode_attn_noalloc",
 )
 
 
@@ -56,6 +56,7 @@ _SIGS = {
     "oasis_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "oasis_sparse_decode_attn_ws": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, ctypes.c_size_t, _P,
                                          _P]),
+    "oasis_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
 }
 
 
@@ -153,6 +154,13 @@ def oasis_sparse_decode_attn_ws(q, pool, table, slots_per_seg, seq_len, B, Hkv, 
     return _check("oasis_sparse_decode_attn_ws", load().oasis_sparse_decode_attn_ws(
         _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
         _ptr(out), _ptr(lse), _ptr(ws), int(ws_bytes), _ptr(status), _stream(stream)))
+
+
+def oasis_sparse_decode_attn_noalloc(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse=None,
+                                     status=None, stream=None):
+    return _check("oasis_sparse_decode_attn_noalloc", load().oasis_sparse_decode_attn_noalloc(
+        _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
+        _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def attn_workspace(B, Hkv, G, D, slots_per_seg, device=None):

@@ -786,4 +786,52 @@ cudaError_t launch_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool
                             counter, st);
 }
 
+// ---- the balanced split without caller memory -------------------------------
+// Scratch for oasis_sparse_decode_attn_noalloc: a file-scope device array, so
+// the call needs no allocation at all.  8 MiB holds the workspace of a split
+// into up to 504 CTAs at 16 query heads per KV head and D = 128 (about a
+// million slot tiles), more with fewer heads; larger shapes are rejected.  One
+// array per device and process: calls that could overlap (different streams)
+// race on it.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch on the current device, looked up once per device.
+static void *noalloc_scratch() {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+cudaError_t launch_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, const int32_t *table,
+                                              int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G,
+                                              int D, float scale, float *out, float *lse, int32_t *status,
+                                              cudaStream_t st) {
+  if (attn_workspace_bytes(B, Hkv, G, D, slots_per_seg) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  void *ws = noalloc_scratch();
+  if (ws == nullptr) return cudaErrorInvalidDevice;
+  // The per-segment arrival counters must start at zero.  Every completed call
+  // leaves them at zero, but one that timed out may not, so clear them on every
+  // call (a memset of 4 bytes per segment, no allocation).
+  const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
+  const size_t parts = static_cast<size_t>(bal_grid(N)) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  const size_t counters_at = (parts + 255) / 256 * 256;
+  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + counters_at, 0,
+                                  static_cast<size_t>(B) * Hkv * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  return launch_sparse_decode_attn_ws(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws,
+                                      status, st);
+}
+
 }  // namespace oasis
