@@ -22,10 +22,12 @@
  *
  * Conventions shared by every entry point
  *   Memory.     The caller allocates and owns every buffer.  The library
- *               allocates no memory and keeps no state between calls (it only
- *               caches, per process, that each kernel's shared-memory limit
- *               was raised).  Device pointers must be device memory or, where
- *               stated, host memory the GPU can address (pinned and mapped).
+ *               allocates no memory and keeps no state between calls, except
+ *               per process: that each kernel's shared-memory limit was
+ *               raised, and for oasis_sparse_decode_attn_noalloc a static
+ *               8 MiB device scratch array and its address.  Device pointers
+ *               must be device memory or, where stated, host memory the GPU
+ *               can address (pinned and mapped).
  *   Execution.  Every call enqueues kernels on `stream` (NULL = the legacy
  *               default stream) and returns without synchronising.  Outputs
  *               are valid once the stream reaches that point.
