@@ -613,19 +613,40 @@ __global__ void __launch_bounds__(kThreads)
         __threadfence();
         for (int idx = tid; idx < G * D; idx += kThreads) {
           const int qc = idx / D, d = idx % D;
-          float M = -INFINITY;
-          for (int64_t c = c_first; c <= c_last; ++c) {
-            const int sl = (N * c / P) / slots == s ? 0 : 1;
-            M = fmaxf(M, __ldcg(part + (c * 2 + sl) * part_floats + qc));
-          }
-          float acc = 0.0f, ls = 0.0f;
-          if (M > -INFINITY) {
-            for (int64_t c = c_first; c <= c_last; ++c) {
-              const int sl = (N * c / P) / slots == s ? 0 : 1;
-              const float *pc = part + (c * 2 + sl) * part_floats;
-              const float f = exp2f(__ldcg(pc + qc) - M);
-              acc += f * __ldcg(pc + 2 * G + idx);
-              ls += f * __ldcg(pc + G + qc);
+          // online merge over the pieces, kBatch at a time: each batch's loads go out
+          // together, so a merge costs a few L2 round trips, not one per piece
+          constexpr int kBatch = 8;
+          float M = -INFINITY, acc = 0.0f, ls = 0.0f;
+          for (int64_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
+            float pm[kBatch], pl[kBatch], po[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int64_t c = c0 + k;
+              pm[k] = -INFINITY;
+              pl[k] = 0.0f;
+              po[k] = 0.0f;
+              if (c <= c_last) {
+                const int sl = (N * c / P) / slots == s ? 0 : 1;
+                const float *pc = part + (c * 2 + sl) * part_floats;
+                pm[k] = __ldcg(pc + qc);
+                pl[k] = __ldcg(pc + G + qc);
+                po[k] = __ldcg(pc + 2 * G + idx);
+              }
+            }
+            float bm = M;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, pm[k]);
+            if (bm > -INFINITY) {
+              const float r = exp2f(M - bm);  // 0 while nothing was valid yet
+              acc *= r;
+              ls *= r;
+#pragma unroll
+              for (int k = 0; k < kBatch; ++k) {
+                const float f = exp2f(pm[k] - bm);
+                acc += f * po[k];
+                ls += f * pl[k];
+              }
+              M = bm;
             }
           }
           const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
