@@ -220,7 +220,12 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": _config(w, {"sample": f"{segs} segments over {args.steps} steps"}),
+            "config": _config(w, {"layers_per_decode_step": args.layers if args.layers > 0 else
+                                  (36 if args.workload == WORKLOAD_ID else w.layers),
+                                  "step": "one pass of the whole path (summary update, scoring, capped selection, "
+                                          "staging, attention) over one layer, by the oracle on the host, one "
+                                          "segment after another",
+                                  "sample": f"{segs} segments over {args.steps} steps"}),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"{segs} segment-steps cycling over {len(setup[2])} segments, "
                                        f"single-threaded numpy oracle, {total_s:.1f} s timed"},
