@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
 // and after a barrier the CTA writes the max over the groups.  The summary
 // chunks a unit's warps share are read through L1 once per warp.
 constexpr int kQG = 4;              // query pairs per warp
-constexpr int kWarpsQGMax = 8;
+constexpr int kWarpsQGMax = 8;      // warps per CTA; the groups of a unit (NG <= 8 for up to 64 queries)
+static_assert((64 / 2 + kQG - 1) / kQG <= kWarpsQGMax, "64 query vectors must fit one CTA's warps");
 
 template <int CH>
 __global__ void __maxnreg__(128)
@@ -388,13 +389,14 @@ cudaError_t launch_qg(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, co
   const int S = B * Hkv;
   const int Nq = G * Nd;
   const int NG = ((Nq + 1) / 2 + kQG - 1) / kQG;
+  if (NG < 1 || NG > kWarpsQGMax) return cudaErrorInvalidValue;  // one warp per group, at most kWarpsQGMax
   const int WB = std::max(1, kWarpsQGMax / NG);
   const int threads = 32 * NG * WB;
   const int ncand = std::max(1, Nb_max - W);
   const int units_per_seg = (ncand + 63) / 64;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
   const size_t per_seg = sizeof(float4) * static_cast<size_t>(D) * NG * kQG;
-  const size_t pm_bytes = sizeof(float) * 64 * kWarpsQGMax;
+  const size_t pm_bytes = sizeof(float) * 64 * (threads / 32);  // one row of partial maxima per warp
   const int qseg_max = static_cast<int>(std::max<size_t>(1, std::min<size_t>(8, (100 * 1024) / per_seg)));
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score_qg<CH>), threads,
