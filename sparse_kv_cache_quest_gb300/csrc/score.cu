@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
   constexpr int NB = blocks_per_lane<NQP>();
   constexpr int kUnit = 32 * NB;  // blocks per warp unit
   constexpr int kFill = 2;        // raw query loads in flight per thread while filling qsm
+  static_assert(CH % kPF == 0, "the chunk loop steps by kPF: it must divide the chunk count");
   extern __shared__ float4 qsm[];  // [qseg][D][NQP/2] {qn_j, qn_j+1, qp_j, qp_j+1}
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t U = static_cast<int64_t>(S) * units_per_seg;
@@ -242,6 +243,7 @@ __global__ void __maxnreg__(128)
                int units_per_seg, int qseg, int NG) {
   constexpr int D = CH * 8;
   constexpr int NB = 2, kUnit = 64, kPF = 2;
+  static_assert(CH % kPF == 0, "the chunk loop steps by kPF: it must divide the chunk count");
   const int npairs = NG * kQG;             // padded query pairs of a segment
   const int per_seg_q = D * npairs;        // float4 entries per segment
   extern __shared__ float4 qsm[];          // [qseg][D][npairs] {qn_j, qn_j+1, qp_j, qp_j+1}
