@@ -53,6 +53,7 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--bg-streams", type=int, default=2, help="background streams, taken by the layers in turn")
+    p.add_argument("--xf-streams", type=int, default=2, help="staging streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
     p.add_argument("--attn", choices=["cluster", "balanced"], default="cluster",
                    help="attention split: per-head thread-block clusters, or SM-balanced with a workspace")
@@ -339,7 +340,8 @@ def run_ours(args):
 
     # ---- the timed region: decode steps through R layers, one CUDA graph each
     step_graph = okv.DecodeStepGraph(insts, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys,
-                                     new_block=w.Nb - 1, n_bg=args.bg_streams, fg_priority=args.fg_priority)
+                                     new_block=w.Nb - 1, n_bg=args.bg_streams, fg_priority=args.fg_priority,
+                                     n_xf=args.xf_streams)
     reps = max(1, -(-args.steps // R))
     layer_steps = reps * R
     for _ in range(max(1, -(-args.warmup // R))):
@@ -437,6 +439,7 @@ def run_ours(args):
                 "config": _config(w, {
                     "layers_per_decode_step": R,
                     "background_streams": args.bg_streams,
+                    "staging_streams": args.xf_streams,
                     "foreground_priority": args.fg_priority,
                     "attention_split": args.attn,
                     "step": "one pass of the whole path (summary update, scoring, capped selection, staging, "
@@ -481,7 +484,8 @@ def _e2e(args, w, insts, host, seg_stride, q, qd, sl, new_keys, world, dev, time
 
     import sparse_kv_cache_quest_gb300 as okv
     g = okv.DecodeStepGraph(insts, q, qd, sl, host, seg_stride, w.Nb, new_keys=new_keys, new_block=w.Nb - 1,
-                            host_io=True, n_bg=args.bg_streams, fg_priority=args.fg_priority)
+                            host_io=True, n_bg=args.bg_streams, fg_priority=args.fg_priority,
+                            n_xf=args.xf_streams)
     R = len(insts)
     g.replay()
     torch.cuda.synchronize()

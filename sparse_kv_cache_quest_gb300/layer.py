@@ -256,11 +256,13 @@ class DecodeStepGraph:
     kernels.  Tables do not
     advance (the new tables stay in ``table_next``).  n_bg: background streams,
     taken by the layers in turn; fg_priority: CUDA stream priority of the
-    foreground stream (lower is higher; 0 = default).
+    foreground stream (lower is higher; 0 = default); n_xf: staging streams,
+    taken by the layers in turn.
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
-                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2, fg_priority: int = 0):
+                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2, fg_priority: int = 0,
+                 n_xf: int = 2):
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
@@ -282,7 +284,12 @@ class DecodeStepGraph:
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
         fg = torch.cuda.Stream(dev, priority=fg_priority)
-        sel, xf = (torch.cuda.Stream(dev) for _ in range(2))
+        sel = torch.cuda.Stream(dev)
+        # staging streams taken by alternate layers: the staging of layer l+1 may
+        # start while layer l's still runs, hiding each copy's start-up and tail
+        # behind its neighbour (the copies are bound by the host link, and a
+        # chain of them on one stream comes close to the step's critical path)
+        xfs = [torch.cuda.Stream(dev) for _ in range(n_xf)]
         # host I/O on copy streams of its own, per layer, so that the copies of one
         # layer overlap the kernels of the others
         h2d, d2h = (torch.cuda.Stream(dev) for _ in range(2)) if host_io else (None, None)
@@ -298,11 +305,12 @@ class DecodeStepGraph:
         def body(cur):
             start = torch.cuda.Event()
             start.record(cur)
-            for st in (fg, sel, xf, *bgs, *copy_streams):
+            for st in (fg, sel, *xfs, *bgs, *copy_streams):
                 st.wait_event(start)
             prev_fg = None
             for i, lay in enumerate(layers):
                 bg = bgs[i % len(bgs)]
+                xf = xfs[i % len(xfs)]
                 if host_io:
                     with torch.cuda.stream(h2d):
                         self.in_dev[i].copy_(self.in_host[i], non_blocking=True)
@@ -334,7 +342,7 @@ class DecodeStepGraph:
                     with torch.cuda.stream(d2h):
                         for h, d in zip(self.host_out[i], outs[i]):
                             h.copy_(d, non_blocking=True)
-            for st in (fg, sel, xf, *bgs, *copy_streams):
+            for st in (fg, sel, *xfs, *bgs, *copy_streams):
                 e = torch.cuda.Event()
                 e.record(st)
                 cur.wait_event(e)
