@@ -59,6 +59,17 @@ constexpr size_t smem_budget() { return 100 * 1024; }
 template <int NQP>
 constexpr int prefetch() { return 2; }  // chunks in flight per lane and block
 
+// Summary chunk loads of k_score: read-only path, no L1 allocation (each chunk
+// is read by one warp once), L2 fetching 256-byte groups (a warp's load covers
+// 512 contiguous bytes).  Measured 0.3 us faster per launch than plain __ldg.
+__device__ __forceinline__ uint4 ld_summary(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // CH = D / 8 chunks of 8 dims (8 for D = 64, 16 for D = 128).
 template <int NQP, int CH>
 __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
@@ -99,8 +110,8 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
     for (int p = 0; p < kPF; ++p)
 #pragma unroll
       for (int i = 0; i < NB; ++i) {
-        bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
-        bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
+        bmn[p][i] = ld_summary(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
+        bmx[p][i] = ld_summary(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
       }
     Lraw = __ldg(seq_len + s / Hkv);
   };
@@ -177,8 +188,8 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
               mn[i] = bmn[cc][i];
               mx[i] = bmx[cc][i];
               if (c + kPF < CH) {
-                bmn[cc][i] = __ldg(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
-                bmx[cc][i] = __ldg(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+                bmn[cc][i] = ld_summary(pmn + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
+                bmx[cc][i] = ld_summary(pmx + static_cast<int64_t>(c + kPF) * Nb_max + bl[i]);
               }
             }
             const float4 *qrow = qbase + (c * 8) * (NQP / 2);
