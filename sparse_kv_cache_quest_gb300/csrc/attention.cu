@@ -53,6 +53,7 @@ constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNST = 2;                    // ring stages per warp
 constexpr int kListMax = 512;              // listed slots per warp
+constexpr int kMaxCluster = 8;             // CTAs per segment in the cluster split
 constexpr uint32_t kWaitTries = 1u << 22;  // bounded mbarrier polls (far beyond any real copy)
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads)
       }
   }
   __syncthreads();
-  for (int idx = tid; idx < GQ * D; idx += kThreads) {
+  for (int idx = tid; idx < G * D; idx += kThreads) {  // the padded columns qc >= G are never read
     const int qc = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
@@ -365,18 +366,36 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   cluster.sync();
-  if (rank == 0) {
-    for (int idx = tid; idx < GQ * D; idx += kThreads) {
+  // Cluster merge: every rank combines its share of the G*D outputs, reading all
+  // ranks' CTA totals through distributed shared memory with a thread's remote
+  // loads issued together (one round trip per output, spread over the cluster).
+  {
+    const int n_out = G * D, per = (n_out + CL - 1) / CL;
+    const int e1 = min(n_out, (rank + 1) * per);
+    for (int idx = rank * per + tid; idx < e1; idx += kThreads) {
       const int qc = idx / D, d = idx % D;
-      if (qc >= G) continue;
+      float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < CL) {
+          mr[r] = cluster.map_shared_rank(cm, r)[qc];
+          lr[r] = cluster.map_shared_rank(cl, r)[qc];
+          orr[r] = cluster.map_shared_rank(co, r)[qc * D + d];
+        }
+      }
       float M = -INFINITY;
-      for (int r = 0; r < CL; ++r) M = fmaxf(M, cluster.map_shared_rank(cm, r)[qc]);
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CL) M = fmaxf(M, mr[r]);
       float acc = 0.0f, ls = 0.0f;
       if (M > -INFINITY) {
-        for (int r = 0; r < CL; ++r) {
-          const float f = exp2f(cluster.map_shared_rank(cm, r)[qc] - M);
-          acc += f * cluster.map_shared_rank(co, r)[qc * D + d];
-          ls += f * cluster.map_shared_rank(cl, r)[qc];
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < CL) {
+            const float f = exp2f(mr[r] - M);
+            acc += f * orr[r];
+            ls += f * lr[r];
+          }
         }
       }
       const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
@@ -384,7 +403,7 @@ __global__ void __launch_bounds__(kThreads)
       if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
     }
   }
-  cluster.sync();
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ---- balanced split with a caller workspace --------------------------------
@@ -704,7 +723,7 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   int CL = static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / S)));
   CL = std::min(CL, slots);
   while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // each warp's list fits
-  if (CL > 8) return cudaErrorInvalidValue;
+  if (CL > kMaxCluster) return cudaErrorInvalidValue;
   LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(kThreads), smem, st);
   cudaLaunchAttribute cl;
   cl.id = cudaLaunchAttributeClusterDimension;
