@@ -410,19 +410,19 @@ def run_ours(args):
                   "note": "the kernel issues two FMAs per term (one adds an exact zero), so it can reach at most 0.5"}
     if dom == "score" and score_alu_bound:
         roof = {"kernel": "k_score (oasis_score_blocks)", "bound": "alu", **score_fp32,
-                "traffic": _traffic("k_score"),
+                "traffic": _traffic("k_score", w),
                 "timing": "CUDA graph of back-to-back launches over the layers' buffer sets, CUDA events",
                 "other": {"attn": {"us": kern["attn"], "gbs": k_gbs["attn"], "frac": k_gbs["attn"] / peak,
-                                   "traffic": _traffic("k_attn")},
+                                   "traffic": _traffic("k_attn", w)},
                           "score_hbm": {"gbs": k_gbs["score"], "frac": k_gbs["score"] / peak}}}
     else:
         roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": "k_score (oasis_score_blocks)"}[dom],
                 "bound": "hbm", "achieved": k_gbs[dom], "peak": peak, "unit": "GB/s", "frac": k_gbs[dom] / peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "traffic": _traffic(kname[dom]),
+                "traffic": _traffic(kname[dom], w),
                 "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes,
                 "timing": "CUDA graph of back-to-back launches over the layers' buffer sets, CUDA events",
-                "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak, "traffic": _traffic(kname[k])}
+                "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak, "traffic": _traffic(kname[k], w)}
                           for k in k_gbs if k != dom}}
         roof["other"]["score_fp32"] = score_fp32
 
@@ -455,11 +455,16 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def _traffic(kernel):
+TRAFFIC_WORKLOAD = "qwen3-8b-layer"  # the workload the committed DRAM-traffic record was captured on
+
+
+def _traffic(kernel, w):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel's current source (else None)."""
+    this workload and on the kernel's current source (else None)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic_qwen3-8b-layer.json")
+    if w.name != TRAFFIC_WORKLOAD:
+        return None
+    path = os.path.join(ROOT, "profiles", f"ncu_dram_traffic_{TRAFFIC_WORKLOAD}.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:

@@ -53,3 +53,20 @@ def test_reference_arm_runs_on_rank0_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(None)          # returns before touching its arguments
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_record_only_for_its_workload_and_current_sources():
+    """The committed DRAM-traffic record applies to the workload it was captured on
+    and only while the kernel sources still hash to what was profiled."""
+    import hashlib
+    import json
+    import os
+    from synth import workload as wl
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", f"ncu_dram_traffic_{bench.TRAFFIC_WORKLOAD}.json")))
+    w_prof = next(w for w in wl.WORKLOADS.values() if w.name == bench.TRAFFIC_WORKLOAD)
+    w_other = next(w for w in wl.WORKLOADS.values() if w.name != bench.TRAFFIC_WORKLOAD)
+    for kernel, r in rec.items():
+        assert bench._traffic(kernel, w_other) is None
+        src = os.path.join(bench.ROOT, "sparse_kv_cache_quest_gb300", "csrc", r["source"])
+        current = hashlib.sha256(open(src, "rb").read()).hexdigest() == r["source_sha256"]
+        assert bench._traffic(kernel, w_prof) == (r["dram_bytes_per_launch"] if current else None)
