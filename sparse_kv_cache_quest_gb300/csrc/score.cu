@@ -41,17 +41,17 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 224;  // 7 warps: two CTAs cover 14 of the 16 warp slots 128 registers allow
+constexpr int kThreads = 256;  // 8 warps: two CTAs fill the 16 warp slots 128 registers allow
 constexpr int kWarps = kThreads / 32;
 
 // Blocks per lane: two while the accumulators fit (each broadcast query load
 // then feeds four packed FMAs instead of two), else one.
 template <int NQP>
 constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
-// Register cap: 128 keeps two 7-warp CTAs per SM (14 of the 16 warp slots the
-// register file allows at 128); the wide query groups take up to 255 with one CTA
-// per SM.  (A 112 cap, which would leave room beside two CTAs for an attention CTA
-// of another layer, spills and measured slower in the pipelined decode step.)
+// Register cap: 128 keeps two 8-warp CTAs per SM (all 16 warp slots the register
+// file allows at 128); the wide query groups take up to 255 with one CTA per SM.
+// (Caps of 112-120, which would leave room beside two CTAs for an attention CTA of
+// another layer, spill and did not speed up the pipelined decode step.)
 template <int NQP>
 constexpr int max_regs() { return NQP <= 12 ? 128 : 255; }
 template <int NQP>
