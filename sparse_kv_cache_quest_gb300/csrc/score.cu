@@ -49,11 +49,12 @@ constexpr int kWarps = kThreads / 32;
 template <int NQP>
 constexpr int blocks_per_lane() { return NQP <= 16 ? 2 : 1; }
 // Register cap: 128 keeps two 8-warp CTAs per SM (all 16 warp slots the register
-// file allows at 128); the wide query groups take up to 255 with one CTA per SM.
+// file allows at 128).  At 16 query vectors the kernel spills a few words under
+// that cap and still runs faster than with one CTA of 154 registers per SM.
 // (Caps of 112-120, which would leave room beside two CTAs for an attention CTA of
 // another layer, spill and did not speed up the pipelined decode step.)
 template <int NQP>
-constexpr int max_regs() { return NQP <= 12 ? 128 : 255; }
+constexpr int max_regs() { return 128; }
 template <int NQP>
 constexpr size_t smem_budget() { return 100 * 1024; }
 template <int NQP>
