@@ -31,7 +31,7 @@
 //
 // More than 16 query vectors (e.g. 16 query heads x 4 drafts): the
 // accumulators of all of them no longer fit two blocks per lane, so k_score_qg
-// splits the query pairs over the warps of a CTA (4 pairs each) and takes the
+// splits the query pairs over the warps of a CTA (8 pairs each) and takes the
 // max over the groups in shared memory; see below.
 #include <algorithm>
 #include <cfloat>
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
 // with 2*kQG query vectors), leave their per-block maxima in shared memory,
 // and after a barrier the CTA writes the max over the groups.  The summary
 // chunks a unit's warps share are read through L1 once per warp.
-constexpr int kQG = 4;              // query pairs per warp
+constexpr int kQG = 8;              // query pairs per warp (4 measured 13 % slower at 64 queries)
 constexpr int kWarpsQGMax = 8;      // warps per CTA; the groups of a unit (NG <= 8 for up to 64 queries)
 static_assert((64 / 2 + kQG - 1) / kQG <= kWarpsQGMax, "64 query vectors must fit one CTA's warps");
 
