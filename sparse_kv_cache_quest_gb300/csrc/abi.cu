@@ -21,8 +21,37 @@ inline int finish(cudaError_t e) { return e == cudaSuccess ? OASIS_OK : OASIS_EC
 namespace oasis {
 
 // SM count and resident CTAs per SM of a kernel at a given dynamic shared-memory
-// size, after raising the kernel's shared-memory limit to that size.  Cached
-// per process, device, kernel, block size and shared-memory size.
+// size, after raising the kernel's shared-memory limit to at least that size.
+// Cached per process, device, kernel, block size and shared-memory size.
+// Raises a kernel's dynamic shared-memory limit to at least `smem` bytes on the
+// current device; never lowers it.  The limit is a property of the function, so
+// a lower value set for a small launch would make a larger launch of the same
+// kernel (an earlier configuration, or a captured graph replayed later) fail.
+cudaError_t raise_smem_limit(const void *fn, size_t smem) {
+  struct Limit {
+    const void *fn;
+    int dev;
+    size_t smem;
+  };
+  static std::mutex mu;
+  static std::vector<Limit> limits;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  Limit *cur = nullptr;
+  for (Limit &x : limits)
+    if (x.fn == fn && x.dev == dev) cur = &x;
+  if (cur != nullptr && cur->smem >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (cur != nullptr)
+    cur->smem = smem;
+  else
+    limits.push_back(Limit{fn, dev, smem});
+  return cudaSuccess;
+}
+
 cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm) {
   struct Entry {
     const void *fn;
@@ -35,6 +64,8 @@ cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  e = raise_smem_limit(fn, smem);  // on every call: a cached geometry does not mean the limit still fits
+  if (e != cudaSuccess) return e;
   {
     std::lock_guard<std::mutex> lk(mu);
     for (const Entry &x : cache)
@@ -46,8 +77,6 @@ cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, 
   }
   int n = 0, p = 0;
   e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p, fn, threads, smem);
   if (e != cudaSuccess) return e;

@@ -124,6 +124,7 @@ struct LaunchCfg {
 
 // Launchers implemented by the kernel translation units (host side).
 namespace oasis {
+cudaError_t raise_smem_limit(const void *fn, size_t smem);
 cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm);
 cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
                                  int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,

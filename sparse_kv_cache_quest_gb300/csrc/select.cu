@@ -350,8 +350,7 @@ cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int
   // static (histograms, scalars) + dynamic shared memory may pass the 48 KiB
   // default before the dynamic part alone does
   if (smem + kStaticSmemBound > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select), smem);
     if (e != cudaSuccess) return e;
   }
   LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);

@@ -136,6 +136,28 @@ def test_scores_bit_exact(D, G, Nd, W):
     assert st.item() == 0
 
 
+def test_scores_configuration_changes_keep_launching():
+    """Launches of one scoring kernel with more, then less, then more dynamic
+    shared memory (query groups of different widths): each must still launch and
+    match the oracle, i.e. the kernel's shared-memory limit never drops below a
+    size an earlier configuration needs."""
+    rng = np.random.default_rng(77)
+    B, Hkv, Nb, D = 1, 2, 200, 128
+    S = B * Hkv
+    lo, hi = _random_summaries(rng, S, Nb, D)
+    lens = torch.tensor([16 * Nb], dtype=torch.int32, device=DEV)
+    for G, Nd in [(10, 4), (16, 4), (10, 4), (6, 3), (16, 4)]:
+        qd = _bf16_rand(rng, (B, Nd, Hkv * G, D))
+        scores = torch.zeros((S, Nb), dtype=torch.float32, device=DEV)
+        okv.oasis_score_blocks(_to_chunk_major(lo), _to_chunk_major(hi), Nb, _dev_bf16(qd), B, Hkv, G, Nd, D, lens,
+                               0, scores, None)
+        torch.cuda.synchronize()
+        got = scores.cpu().numpy()
+        for s in range(S):
+            ref = oscore.score_blocks(lo[s], hi[s], oscore.segment_queries(qd, 0, s, G))
+            assert np.array_equal(got[s].view(np.uint32), ref.view(np.uint32)), (G, Nd, s)
+
+
 def test_scores_golden_toy_and_order_case():
     with open(os.path.join(GOLDEN, "score_toy.json")) as f:
         g = json.load(f)
