@@ -27,9 +27,10 @@
 // 8x8 transpose per half (movmatrix), and is split into bf16 hi + lo parts so
 // that the PV product keeps about 16 significant bits of p.  Each thread owns
 // whole output elements, so no cross-lane reduction is needed per slot.
-// Warps combine through shared memory (reusing the rings), then the CL CTAs of
-// the cluster combine through distributed shared memory into rank 0, which
-// writes out and lse.  No global scratch memory is used.
+// Warps combine through shared memory (reusing the rings), then every CTA of
+// the cluster combines a 1/CL share of the outputs from all CL CTAs' totals
+// through distributed shared memory and writes it to out and lse.  No global
+// scratch memory is used.
 //
 // k_attn_bal (further down) is the alternative split over all segments' slots
 // with a caller workspace; it measured slower than the cluster split on the

@@ -14,8 +14,8 @@
 // No reassociation, no fast-math: the result is bit-identical to a plain loop.
 //
 // Work split.  The unit of work is 32*NB consecutive candidate blocks of one
-// segment, NB blocks per lane of a warp (NB = 2 while the accumulators fit).  Units are numbered segment-major and
-// each CTA of a persistent grid (SM count x resident CTAs per SM) takes one
+// segment, NB = 2 blocks per lane of a warp.  Units are numbered segment-major
+// and each CTA of a persistent grid (SM count x resident CTAs per SM) takes one
 // contiguous range of units, so every SM gets the same number of units (+-1)
 // whatever the segment count.  A CTA walks the segments of its range in phases
 // of at most `qseg` segments whose query operands it holds in shared memory;
@@ -26,8 +26,8 @@
 // per load) with kPF chunks in flight.  Per dim it widens kmin/kmax to fp32 and
 // runs two packed fp32x2 FMAs (fma.rn.f32x2) per pair of queries and block:
 // the query operands sit in shared memory as {qn_j, qn_j+1, qp_j, qp_j+1}, one
-// broadcast 16-byte load per pair and dim feeding 2*NB packed FMAs.  Queries are padded to NQP by repeating the
-// last one, which leaves the max unchanged.
+// broadcast 16-byte load per pair and dim feeding 2*NB packed FMAs.  Queries
+// are padded to NQP by repeating the last one, which leaves the max unchanged.
 //
 // More than 16 query vectors (e.g. 16 query heads x 4 drafts): the
 // accumulators of all of them no longer fit two blocks per lane, so k_score_qg
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
   }
 }
 
-// ---- wide query groups (Nq > 12) ------------------------------------------
+// ---- wide query groups (Nq > 16) ------------------------------------------
 // The padded query pairs of a KV head are split into NG groups of kQG pairs.
 // A round of a CTA takes WB consecutive units of 64 blocks; the NG warps of a
 // unit score its blocks against one group each (the same inner loop as above,
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
 // and after a barrier the CTA writes the max over the groups.  The summary
 // chunks a unit's warps share are read through L1 once per warp.
 constexpr int kQG = 8;              // query pairs per warp (4 measured 13 % slower at 64 queries)
-constexpr int kWarpsQGMax = 8;      // warps per CTA; the groups of a unit (NG <= 8 for up to 64 queries)
+constexpr int kWarpsQGMax = 8;      // warps per CTA (NG <= 4 groups of a unit for up to 64 queries)
 static_assert((64 / 2 + kQG - 1) / kQG <= kWarpsQGMax, "64 query vectors must fit one CTA's warps");
 
 template <int CH>
