@@ -253,11 +253,10 @@ class DecodeStepGraph:
     copy) before that layer's work and each layer's results (out, lse, new
     table, plan, plan counts) back to pinned host memory (``host_out[i]``) once
     they exist, on two copy streams, so the copies overlap other layers'
-    kernels.  Tables do not
-    advance (the new tables stay in ``table_next``).  n_bg: background streams,
-    taken by the layers in turn; fg_priority: CUDA stream priority of the
-    foreground stream (lower is higher; 0 = default); n_xf: staging streams,
-    taken by the layers in turn.
+    kernels.  Tables do not advance (the new tables stay in ``table_next``).
+    n_bg: background streams, taken by the layers in turn; fg_priority: CUDA
+    stream priority of the foreground stream (lower is higher; 0 = default);
+    n_xf: staging streams, taken by the layers in turn.
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
