@@ -52,7 +52,7 @@ def _args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget (CPU baseline)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--bg-streams", type=int, default=2, help="background streams, taken by the layers in turn")
+    p.add_argument("--bg-streams", type=int, default=3, help="background streams, taken by the layers in turn")
     p.add_argument("--xf-streams", type=int, default=2, help="staging streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
     p.add_argument("--attn", choices=["cluster", "balanced"], default="cluster",

@@ -240,8 +240,8 @@ class DecodeStepGraph:
     """One decode step through several layers as one CUDA graph, pipelined
     across layers as in the asynchronous prefetch pipeline of the OasisKV paper
     review (xllm-io), §3 Fig. 8 and eq. (4): the foreground attends layer after
-    layer on one stream; the background of layer l (summary update + scoring,
-    then selection, then staging) starts once the foreground has reached layer l
+    layer on one stream; the background of layer l (summary update, scoring and
+    selection on one stream, then staging) starts once the foreground has reached layer l
     (its draft queries exist) and overlaps the attention of the following
     layers; the staging of layer l waits for layer l's attention (it overwrites
     slots that attention reads) and must end before the next step, where the
@@ -260,7 +260,7 @@ class DecodeStepGraph:
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
-                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 2, fg_priority: int = 0,
+                 new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 3, fg_priority: int = 0,
                  n_xf: int = 2):
         dev = layers[0].device
         self.layers = layers
@@ -283,7 +283,6 @@ class DecodeStepGraph:
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
         fg = torch.cuda.Stream(dev, priority=fg_priority)
-        sel = torch.cuda.Stream(dev)
         # staging streams taken by alternate layers: the staging of layer l+1 may
         # start while layer l's still runs, hiding each copy's start-up and tail
         # behind its neighbour (the copies are bound by the host link, and a
@@ -292,10 +291,10 @@ class DecodeStepGraph:
         # host I/O on copy streams of its own, per layer, so that the copies of one
         # layer overlap the kernels of the others
         h2d, d2h = (torch.cuda.Stream(dev) for _ in range(2)) if host_io else (None, None)
-        # two background streams taken by alternate layers: the background of
-        # layer l+1 needs only the foreground to have passed layer l, so it may
-        # start while layer l's scoring still runs, which hides each scoring
-        # kernel's start-up and tail behind its neighbour
+        # background streams taken by the layers in turn (three by default): the
+        # background of layer l+1 needs only the foreground to have passed layer
+        # l, so it may start while layer l's scoring or selection still runs,
+        # which hides each kernel's start-up and tail behind its neighbours
         bgs = [torch.cuda.Stream(dev) for _ in range(n_bg)]
         stage_args = (host_kv, host_seg_stride_bytes, host_nb)
 
@@ -304,7 +303,7 @@ class DecodeStepGraph:
         def body(cur):
             start = torch.cuda.Event()
             start.record(cur)
-            for st in (fg, sel, *xfs, *bgs, *copy_streams):
+            for st in (fg, *xfs, *bgs, *copy_streams):
                 st.wait_event(start)
             prev_fg = None
             for i, lay in enumerate(layers):
@@ -322,12 +321,9 @@ class DecodeStepGraph:
                 if new_keys is not None:
                     lay.build_summary(self.new_keys[i], self.seq_len, blk_begin=new_block, blk_count=1, stream=bg)
                 lay.score(self.qdraft[i], self.seq_len, stream=bg)
-                e_sc = torch.cuda.Event()
-                e_sc.record(bg)
-                sel.wait_event(e_sc)
-                lay.select(self.seq_len, stream=sel)
+                lay.select(self.seq_len, stream=bg)
                 e_sel = torch.cuda.Event()
-                e_sel.record(sel)
+                e_sel.record(bg)
                 lay.attend(self.q[i], self.seq_len, stream=fg)
                 e_fg = torch.cuda.Event()
                 e_fg.record(fg)
@@ -341,7 +337,7 @@ class DecodeStepGraph:
                     with torch.cuda.stream(d2h):
                         for h, d in zip(self.host_out[i], outs[i]):
                             h.copy_(d, non_blocking=True)
-            for st in (fg, sel, *xfs, *bgs, *copy_streams):
+            for st in (fg, *xfs, *bgs, *copy_streams):
                 e = torch.cuda.Event()
                 e.record(st)
                 cur.wait_event(e)
