@@ -375,7 +375,10 @@ def run_ours(args):
              "select": lambda lay, st_: lay.select(sl, stream=st_),
              "stage": lambda lay, st_: lay.stage(host, seg_stride, w.Nb, stream=st_),
              "summary_update": lambda lay, st_: lay.build_summary(new_keys, sl, blk_begin=w.Nb - 1, blk_count=1,
-                                                                  stream=st_)}
+                                                                  stream=st_),
+             # the full build at sparsification time (not part of a decode step): every block's keys
+             "summary_full_build": lambda lay, st_: lay.build_summary(tiles, sl, 0, w.Nb, strides=strides,
+                                                                      stream=st_)}
     n_launch = max(8, R)
     for name, fn in calls.items():
         side = torch.cuda.Stream(dev)
@@ -425,6 +428,12 @@ def run_ours(args):
                 "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak, "traffic": _traffic(kname[k], w)}
                           for k in k_gbs if k != dom}}
         roof["other"]["score_fp32"] = score_fp32
+    # full summary build: reads the keys of every block (16 tokens x D bf16), writes kmin and kmax
+    build_bytes = w.S * w.Nb * (16 * w.D * 2 + 2 * w.D * 2)
+    build_gbs = build_bytes / (kern["summary_full_build"] * 1e-6) / 1e9
+    roof["other"]["summary_full_build"] = {"us": kern["summary_full_build"], "gbs": build_gbs,
+                                           "frac": build_gbs / peak, "algorithmic_bytes_per_launch": build_bytes,
+                                           "traffic": _traffic("k_build_summary_full", w)}
 
     e2e = None
     if not args.no_e2e:
