@@ -226,19 +226,6 @@ __global__ void __launch_bounds__(kThreads)
     fence_mbar_init();
   }
 
-  // Q^T B-fragments: column n = query head nt*8 + g, rows k = dims 16ks + 2t (+1, +8, +9)
-  uint32_t qb[NT][KS][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int qi = nt * 8 + g;
-    const uint32_t *row =
-        reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bseq) * Hq + h * G + qi) * D);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qb[nt][ks][0] = qi < G ? row[(16 * ks + 2 * t) >> 1] : 0u;
-      qb[nt][ks][1] = qi < G ? row[(16 * ks + 8 + 2 * t) >> 1] : 0u;
-    }
-  }
   float o[NT][KS][4];
   float m[NT][2], l[NT][2];
 #pragma unroll
@@ -283,6 +270,21 @@ __global__ void __launch_bounds__(kThreads)
   };
   if (lane == 0)
     for (int c = 0; c < kNST && c < count; ++c) issue(c, c);
+
+  // Q^T B-fragments: column n = query head nt*8 + g, rows k = dims 16ks + 2t (+1, +8, +9);
+  // loaded once the first tile copies are in flight, so they overlap the copies
+  uint32_t qb[NT][KS][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int qi = nt * 8 + g;
+    const uint32_t *row =
+        reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bseq) * Hq + h * G + qi) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[nt][ks][0] = qi < G ? row[(16 * ks + 2 * t) >> 1] : 0u;
+      qb[nt][ks][1] = qi < G ? row[(16 * ks + 8 + 2 * t) >> 1] : 0u;
+    }
+  }
   int issued = min(kNST, count), consumed = 0;
   bool timed_out = false;
 
