@@ -271,11 +271,36 @@ __global__ void __maxnreg__(128)
   const int s_last = static_cast<int>((u1 - 1) / units_per_seg);
   const int max_tokens = Nb_max * kBlockTokens;
 
+  // State of the warp's current unit, as in k_score: its first kPF chunks and its
+  // sequence length are requested as soon as the unit is known (before the
+  // previous round's merge), block rows clamped to the summary capacity.
+  int s = 0, base = 0, Lraw = 0;
+  int bl[NB];
+  const uint4 *pmn = nullptr, *pmx = nullptr;
+  uint4 bmn[kPF][NB], bmx[kPF][NB];
+  auto start_unit = [&](int64_t u) {
+    s = static_cast<int>(u / units_per_seg);
+    base = static_cast<int>(u % units_per_seg) * kUnit;
+#pragma unroll
+    for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, Nb_max - 1);
+    pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
+    pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
+#pragma unroll
+    for (int p = 0; p < kPF; ++p)
+#pragma unroll
+      for (int i = 0; i < NB; ++i) {
+        bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
+        bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
+      }
+    Lraw = __ldg(seq_len + s / Hkv);
+  };
+
   for (int s_lo = static_cast<int>(u0 / units_per_seg); s_lo <= s_last; s_lo += qseg) {
     const int s_hi = min(s_last + 1, s_lo + qseg);
     const int64_t pu0 = std::max(u0, static_cast<int64_t>(s_lo) * units_per_seg);
     const int64_t pu1 = std::min(u1, static_cast<int64_t>(s_hi) * units_per_seg);
     __syncthreads();  // the previous phase is done with qsm
+    if (ub < WB && pu0 + ub < pu1) start_unit(pu0 + ub);
     const int n_items = (s_hi - s_lo) * CH * nqv;
     for (int idx = tid; idx < n_items; idx += nthreads) {
       const int sl = idx / (CH * nqv), rem = idx % (CH * nqv), c = rem / nqv, j = rem % nqv;
@@ -299,31 +324,19 @@ __global__ void __maxnreg__(128)
       const int64_t u = r0 + ub;
       float best[NB] = {-FLT_MAX, -FLT_MAX};
       if (ub < WB && u < pu1) {
-        const int s = static_cast<int>(u / units_per_seg);
-        const int base = static_cast<int>(u % units_per_seg) * kUnit;
-        const int L = load_len(seq_len, s / Hkv, max_tokens, status,
-                               lane == 0 && grp == 0 && base == 0 && (s % Hkv) == 0);
+        int L = Lraw;
+        if (L < 0 || L > max_tokens) {
+          if (lane == 0 && grp == 0 && base == 0 && (s % Hkv) == 0) report(status, OASIS_STATUS_SEQ_LEN);
+          L = L < 0 ? 0 : max_tokens;
+        }
         const int nc = ceil_div(L, kBlockTokens) - W;
         if (base < nc) {  // warp-uniform
-          int bl[NB];
-#pragma unroll
-          for (int i = 0; i < NB; ++i) bl[i] = min(base + lane + 32 * i, nc - 1);
-          const uint4 *pmn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max;
-          const uint4 *pmx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max;
           const float4 *qbase = qsm + (s - s_lo) * per_seg_q + grp * kQG;
           unsigned long long acc[NB][kQG];
 #pragma unroll
           for (int i = 0; i < NB; ++i)
 #pragma unroll
             for (int jp = 0; jp < kQG; ++jp) acc[i][jp] = 0ull;  // (+0, +0)
-          uint4 bmn[kPF][NB], bmx[kPF][NB];
-#pragma unroll
-          for (int p = 0; p < kPF; ++p)
-#pragma unroll
-            for (int i = 0; i < NB; ++i) {
-              bmn[p][i] = __ldg(pmn + static_cast<int64_t>(p) * Nb_max + bl[i]);
-              bmx[p][i] = __ldg(pmx + static_cast<int64_t>(p) * Nb_max + bl[i]);
-            }
 #pragma unroll 1
           for (int c0 = 0; c0 < CH; c0 += kPF)
 #pragma unroll
@@ -373,6 +386,8 @@ __global__ void __maxnreg__(128)
               best[i] = fmaxf(best[i], fmaxf(a0, a1));
             }
         }
+        // the next round's unit: its loads overlap this round's merge
+        if (u + WB < pu1) start_unit(u + WB);
       }
 #pragma unroll
       for (int i = 0; i < NB; ++i) pm[warp * kUnit + lane + 32 * i] = best[i];
@@ -380,15 +395,15 @@ __global__ void __maxnreg__(128)
       for (int t = tid; t < WB * kUnit; t += nthreads) {
         const int64_t uu = r0 + t / kUnit;
         if (uu >= pu1) continue;
-        const int s = static_cast<int>(uu / units_per_seg);
+        const int su = static_cast<int>(uu / units_per_seg);
         const int b = static_cast<int>(uu % units_per_seg) * kUnit + t % kUnit;
-        int L = __ldg(seq_len + s / Hkv);
-        L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
-        if (b >= ceil_div(L, kBlockTokens) - W) continue;
+        int Lu = __ldg(seq_len + su / Hkv);
+        Lu = Lu < 0 ? 0 : (Lu > max_tokens ? max_tokens : Lu);
+        if (b >= ceil_div(Lu, kBlockTokens) - W) continue;
         const float *col = pm + (t / kUnit) * NG * kUnit + t % kUnit;
         float m = col[0];
         for (int gq = 1; gq < NG; ++gq) m = fmaxf(m, col[gq * kUnit]);
-        scores[static_cast<int64_t>(s) * Nb_max + b] = m;
+        scores[static_cast<int64_t>(su) * Nb_max + b] = m;
       }
       __syncthreads();  // pm is rewritten next round
     }
