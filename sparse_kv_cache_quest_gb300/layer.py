@@ -253,15 +253,23 @@ class DecodeStepGraph:
     copy) before that layer's work and each layer's results (out, lse, new
     table, plan, plan counts) back to pinned host memory (``host_out[i]``) once
     they exist, on two copy streams, so the copies overlap other layers'
-    kernels.  Tables do not advance (the new tables stay in ``table_next``).
+    kernels.  share_host_inputs: all layers copy their inputs from one pinned
+    host buffer (``host_in[0]``; the bytes moved are the same, the host memory
+    held is one layer's).
+    advance: after its staging, each layer's new table becomes its current
+    table (a device copy of ``table_next`` into ``table``), so that successive
+    replays are successive decode steps; without it the tables do not advance
+    (the new tables stay in ``table_next``).
     n_bg: background streams, taken by the layers in turn; fg_priority: CUDA
     stream priority of the foreground stream (lower is higher; 0 = default);
     n_xf: staging streams, taken by the layers in turn.
+    warmup: run the step once outside the capture first (the step then really
+    runs: with advance, the tables move on by one step).
     """
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
                  new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 3, fg_priority: int = 0,
-                 n_xf: int = 2):
+                 n_xf: int = 2, advance: bool = False, share_host_inputs: bool = False, warmup: bool = True):
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
@@ -269,11 +277,11 @@ class DecodeStepGraph:
         # new keys), so host I/O moves them with a single copy
         srcs = [q, qdraft] + ([new_keys] if new_keys is not None else [])
         self.in_dev, self.in_host, views = [], [], []
-        for _ in layers:
+        for i, _ in enumerate(layers):
             arena, v = _arena(srcs, dev)
             self.in_dev.append(arena)
             views.append(v)
-            if host_io:
+            if host_io and (i == 0 or not share_host_inputs):
                 self.in_host.append(arena.cpu().pin_memory())
         self.q = [v[0] for v in views]
         self.qdraft = [v[1] for v in views]
@@ -311,7 +319,7 @@ class DecodeStepGraph:
                 xf = xfs[i % len(xfs)]
                 if host_io:
                     with torch.cuda.stream(h2d):
-                        self.in_dev[i].copy_(self.in_host[i], non_blocking=True)
+                        self.in_dev[i].copy_(self.in_host[0 if share_host_inputs else i], non_blocking=True)
                     e_in = torch.cuda.Event()
                     e_in.record(h2d)
                     bg.wait_event(e_in)
@@ -337,6 +345,9 @@ class DecodeStepGraph:
                     with torch.cuda.stream(d2h):
                         for h, d in zip(self.host_out[i], outs[i]):
                             h.copy_(d, non_blocking=True)
+                if advance:                                    # after this layer's attention and staging
+                    with torch.cuda.stream(xf):
+                        lay.table.copy_(lay.table_next, non_blocking=True)
             for st in (fg, *xfs, *bgs, *copy_streams):
                 e = torch.cuda.Event()
                 e.record(st)
@@ -344,14 +355,15 @@ class DecodeStepGraph:
 
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            body(side)                                   # warm-up outside capture
-        torch.cuda.current_stream(dev).wait_stream(side)
-        torch.cuda.synchronize(dev)
+        if warmup:
+            with torch.cuda.stream(side):
+                body(side)                               # warm-up outside capture
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize(dev)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph, stream=side):
             body(side)
-        self.h2d_bytes = sum(t.numel() for t in (self.host_in or []))
+        self.h2d_bytes = sum(t.numel() for t in self.in_dev) if host_io else 0
         self.d2h_bytes = sum(t.numel() * t.element_size() for x in (self.host_out or []) for t in x)
 
     def replay(self):

@@ -53,19 +53,19 @@ def _resident(table: torch.Tensor, K: int, nc: int) -> torch.Tensor:
 
 
 def run(ratio: str, K: int, steps: int, dev) -> dict:
-    w = wl.WORKLOADS[2].with_(K=K, fetch_ratio=ratio, drift=2, steps=steps)
+    w = wl.WORKLOADS[2].with_(K=K, fetch_ratio=ratio, drift=2, steps=steps, plant_gain=8.0)
     nc, S = w.nc, w.S
     shape = LayerShape(B=w.B, Hkv=w.Hkv, G=w.G, D=w.D, Nb_max=w.Nb, K=w.K, W=w.W, cap=w.cap, Nd=w.Nd)
     lay = DecodeLayer(shape, device=dev)
     sl = wl.seq_lens(w).to(dev)
-    q = wl.q_true(w, 0).to(dev)
     true_scores = torch.empty((S, w.Nb), dtype=torch.float32, device=dev)
     tiles = torch.empty((S, w.Nb, 2, 16, w.D), dtype=torch.bfloat16, device=dev)
+    for s0 in range(0, S, 8):
+        tiles[s0:s0 + 8] = wl.kv_tiles(w, 0, list(range(s0, min(S, s0 + 8))), device=dev)
+    lay.build_summary(tiles, sl, 0, w.Nb, strides=(tiles.stride(0), tiles.stride(1), tiles.stride(3)))
     stats = {"fetched": [], "cap_binds": [], "draft_true_overlap": [], "resident_recall": [], "admission": []}
     for step in range(steps):
-        for s0 in range(0, S, 8):
-            tiles[s0:s0 + 8] = wl.kv_tiles(w, 0, list(range(s0, min(S, s0 + 8))), device=dev, step=step)
-        lay.build_summary(tiles, sl, 0, w.Nb, strides=(tiles.stride(0), tiles.stride(1), tiles.stride(3)))
+        q = wl.q_true(w, 0, step).to(dev)
         ob.oasis_score_blocks(lay.kmin, lay.kmax, w.Nb, q.view(w.B, 1, w.Hq, w.D), w.B, w.Hkv, w.G, 1, w.D, sl,
                               w.W, true_scores, lay.status)
         t_true = _topk_sets(true_scores, nc, K)

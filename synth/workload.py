@@ -14,6 +14,17 @@ resident set that overlaps the true-query top-K by about 90 % - is assembled by
 ``prior_from_topk`` from a top-K list that the caller computes with its own
 implementation (the oracle in tests, the kernels in the benchmark).
 
+Drift over decode steps (workloads with ``drift > 0``).  Keys and values are
+written once, as in a real decode where the cache never changes after a token
+is written; what moves is where the current query looks.  Step t of the
+``steps`` simulated steps has its own heavy-block positions P_t (each block of
+P_{t-1} moved by +drift or -drift) and its own random unit direction u_t per
+(sequence, KV head).  Every key of a block in P_t gets ``plant_gain * u_t``;
+the true query of step t leans towards u_t (``query_lean * u_t`` added to every
+query head of the group), so the blocks of P_t are the heavy ones at step t.
+The drafts of step t stand in for the speculative queries of the next token:
+they are the true query of step t + 1 (cyclically) plus noise.
+
 Tensor layouts (bf16 tensors use torch.bfloat16):
     keys / values      [S_sel][Nb][16][D]   (S_sel = the requested segments)
     kv tiles           [S_sel][Nb][2][16][D] (K tile, then V tile, per block)
@@ -35,7 +46,7 @@ from . import rng
 BLOCK = 16  # tokens per logical KV block
 
 # stream tags
-T_KEYS, T_VALUES, T_QTRUE, T_QNOISE, T_PLANTS, T_OUTLIERS, T_PRIOR, T_DRIFT, T_MISC = range(1, 10)
+T_KEYS, T_VALUES, T_QTRUE, T_QNOISE, T_PLANTS, T_OUTLIERS, T_PRIOR, T_DRIFT, T_MISC, T_DIRECTION = range(1, 11)
 
 
 @dataclass(frozen=True)
@@ -60,6 +71,7 @@ class Workload:
     drift: int = 0            # heavy blocks move by +-drift blocks per step
     draft_noise: float = 0.3  # std of the noise added to the true query for each draft
     plant_gain: float = 2.0   # planted keys get += plant_gain * unit(sum of the group's true q)
+    query_lean: float = 2.0   # drifting workloads: the true query of step t gets += query_lean * u_t
 
     @property
     def Hq(self) -> int:
@@ -118,7 +130,7 @@ WORKLOADS = {
                 fetch_ratio="0.05", plants=64, outliers=4, outlier_scale=8.0, prior="topk90", seed=1004),
     5: Workload("qwen3-235b-attn", layers=94, B=64, Hkv=4, G=16, D=128, L=32768, K=128, W=0, Nd=4,
                 fetch_ratio="0.05", plants=64, outliers=0, outlier_scale=1.0, prior="topk90", seed=1005,
-                steps=8, drift=2),
+                steps=8, drift=2, plant_gain=8.0),
 }
 
 
@@ -135,23 +147,48 @@ def ragged_seq_lens(w: Workload, min_len: int) -> torch.Tensor:
 
 # ----------------------------------------------------------------------------- queries
 
-def q_true(w: Workload, layer: int) -> torch.Tensor:
-    """True decode query, bf16 [B][Hq][D] (CPU)."""
+def _q_base(w: Workload, layer: int) -> torch.Tensor:
     n = w.B * w.Hq * w.D
     idx = torch.arange(n, dtype=torch.int64) + layer * n
     return rng.normal_bf16(w.seed, T_QTRUE, idx).view(w.B, w.Hq, w.D)
 
 
-def drafts(w: Workload, layer: int, step: int = 0) -> torch.Tensor:
-    """Draft queries bf16 [B][Nd][Hq][D]: bf16(fp32(q_true) + draft_noise * noise) (CPU).
+def q_true(w: Workload, layer: int, step: int = 0) -> torch.Tensor:
+    """True decode query, bf16 [B][Hq][D] (CPU).
 
-    Draft j of step ``step`` draws its own noise; the true query is shared.
+    Without drift the same at every step.  With drift, step t's query is
+    bf16(fp32(base) + query_lean * u_t) with u_t = ``drift_direction(w, layer, t)``
+    of the query head's KV head (t taken modulo ``steps``).
     """
-    qt = q_true(w, layer).to(torch.float32)
+    base = _q_base(w, layer)
+    if w.drift == 0:
+        return base
+    u = drift_direction(w, layer, step % w.steps).repeat_interleave(w.G, dim=1)      # [B][Hq][D]
+    lean = torch.tensor(w.query_lean, dtype=torch.float32)
+    return (base.to(torch.float32) + lean * u).to(torch.bfloat16)
+
+
+def drafts(w: Workload, layer: int, step: int = 0) -> torch.Tensor:
+    """Draft queries bf16 [B][Nd][Hq][D]: bf16(fp32(target) + draft_noise * noise) (CPU).
+
+    Draft j of step ``step`` draws its own noise.  The target is the true query
+    of the same step without drift, and of the next step (cyclically) with
+    drift: the drafts look one token ahead.
+    """
+    target = q_true(w, layer, (step + 1) % w.steps if w.drift else 0).to(torch.float32)
     n = w.B * w.Nd * w.Hq * w.D
     idx = torch.arange(n, dtype=torch.int64) + (layer * w.steps + step) * n
     noise = rng.normal_f32(w.seed, T_QNOISE, idx).view(w.B, w.Nd, w.Hq, w.D)
-    return (qt[:, None, :, :] + torch.tensor(w.draft_noise, dtype=torch.float32) * noise).to(torch.bfloat16)
+    return (target[:, None, :, :] + torch.tensor(w.draft_noise, dtype=torch.float32) * noise).to(torch.bfloat16)
+
+
+def drift_direction(w: Workload, layer: int, step: int) -> torch.Tensor:
+    """Random unit directions u_t, fp32 [B][Hkv][D] (CPU): one per (sequence, KV
+    head) and step; normalised in float64, then rounded once to fp32."""
+    n = w.B * w.Hkv * w.D
+    idx = torch.arange(n, dtype=torch.int64) + (layer * w.steps + step) * n
+    v = rng.normal_f32(w.seed, T_DIRECTION, idx).to(torch.float64).view(w.B, w.Hkv, w.D)
+    return (v / torch.linalg.vector_norm(v, dim=-1, keepdim=True)).to(torch.float32)
 
 
 def plant_direction(w: Workload, layer: int) -> torch.Tensor:
@@ -159,7 +196,7 @@ def plant_direction(w: Workload, layer: int) -> torch.Tensor:
 
     Computed in float64 from the bf16 queries, then rounded once to fp32.
     """
-    qt = q_true(w, layer).to(torch.float64).view(w.B, w.Hkv, w.G, w.D).sum(dim=2)
+    qt = _q_base(w, layer).to(torch.float64).view(w.B, w.Hkv, w.G, w.D).sum(dim=2)
     nrm = torch.linalg.vector_norm(qt, dim=-1, keepdim=True)
     return (qt / nrm).to(torch.float32)
 
@@ -174,11 +211,17 @@ def planted_blocks(w: Workload, layer: int, s: int, step: int = 0) -> torch.Tens
     -drift (a random sign per block and step), clamped into [0, nc); a block
     that would land on another heavy block of the same step stays where it is.
     """
+    return planted_blocks_steps(w, layer, s, step + 1)[step]
+
+
+def planted_blocks_steps(w: Workload, layer: int, s: int, n_steps: int) -> list:
+    """``planted_blocks`` of steps 0 .. n_steps - 1 of segment ``s``, in one pass."""
     if w.plants == 0 or w.nc <= 0:
-        return torch.zeros(0, dtype=torch.int64)
+        return [torch.zeros(0, dtype=torch.int64)] * n_steps
     p = min(w.plants, w.nc)
     cur = rng.random_subset(w.seed, T_PLANTS, (layer * w.S + s) * w.Nb, w.nc, p)
-    for st in range(1, step + 1):
+    out = [cur]
+    for st in range(1, n_steps):
         base = ((layer * w.S + s) * w.steps + st) * w.plants
         signs = rng.random_signs(w.seed, T_DRIFT, torch.arange(base, base + p, dtype=torch.int64))
         taken = set(cur.tolist())
@@ -192,7 +235,8 @@ def planted_blocks(w: Workload, layer: int, s: int, step: int = 0) -> torch.Tens
             else:
                 nxt.append(blk)
         cur = torch.tensor(sorted(nxt), dtype=torch.int64)
-    return cur
+        out.append(cur)
+    return out
 
 
 def outlier_channels(w: Workload, layer: int, h: int) -> torch.Tensor:
@@ -210,32 +254,38 @@ def _segment_index(w: Workload, layer: int, segs: torch.Tensor, device) -> torch
     return base[:, None] + torch.arange(per_seg, dtype=torch.int64, device=device)[None, :]
 
 
-def keys(w: Workload, layer: int, segs, device="cpu", step: int = 0) -> torch.Tensor:
+def keys(w: Workload, layer: int, segs, device="cpu") -> torch.Tensor:
     """Keys bf16 [len(segs)][Nb][16][D] of the requested segments, on ``device``.
 
     Base values are N(0, 1) stand-ins; on the outlier channels of the segment's
     KV head they are multiplied by ``outlier_scale`` (exact: a power of 2); every
     key of a planted block then gets ``plant_gain * u`` added in fp32 and is
-    rounded to bf16 (u from ``plant_direction``).  Tokens past L in a partial
-    last block are generated like the others.
+    rounded to bf16.  Without drift u is ``plant_direction`` and the planted
+    blocks are those of step 0; with drift, for every step t the blocks of step
+    t get ``plant_gain * u_t`` (``drift_direction``), added in step order.
+    Tokens past L in a partial last block are generated like the others.
     """
     segs = torch.as_tensor(segs, dtype=torch.int64).reshape(-1)
     idx = _segment_index(w, layer, segs, device)
     k = rng.normal_bf16(w.seed, T_KEYS, idx).view(len(segs), w.Nb, BLOCK, w.D)
     if w.outliers == 0 and w.plants == 0:
         return k
-    u = plant_direction(w, layer) if w.plants else None
+    if w.plants:
+        dirs = ([drift_direction(w, layer, t) for t in range(w.steps)] if w.drift
+                else [plant_direction(w, layer)])
     kf = k.to(torch.float32)
+    gain = torch.tensor(w.plant_gain, dtype=torch.float32)
     for i, s in enumerate(segs.tolist()):
         b, h = divmod(s, w.Hkv)
         ch = outlier_channels(w, layer, h)
         if len(ch):
             kf[i, :, :, ch.to(device)] *= w.outlier_scale
         if w.plants:
-            pb = planted_blocks(w, layer, s, step).to(device)
-            if len(pb):
-                shift = (torch.tensor(w.plant_gain, dtype=torch.float32) * u[b, h]).to(device)
-                kf[i, pb] = kf[i, pb] + shift
+            pbs = planted_blocks_steps(w, layer, s, len(dirs))
+            for u, pb in zip(dirs, pbs):
+                pb = pb.to(device)
+                if len(pb):
+                    kf[i, pb] = kf[i, pb] + (gain * u[b, h]).to(device)
     return kf.to(torch.bfloat16)
 
 
@@ -246,9 +296,9 @@ def values(w: Workload, layer: int, segs, device="cpu") -> torch.Tensor:
     return rng.normal_bf16(w.seed, T_VALUES, idx).view(len(segs), w.Nb, BLOCK, w.D)
 
 
-def kv_tiles(w: Workload, layer: int, segs, device="cpu", step: int = 0) -> torch.Tensor:
+def kv_tiles(w: Workload, layer: int, segs, device="cpu") -> torch.Tensor:
     """Full KV cache of the segments in tile layout, bf16 [len(segs)][Nb][2][16][D]."""
-    return torch.stack([keys(w, layer, segs, device, step), values(w, layer, segs, device)], dim=2)
+    return torch.stack([keys(w, layer, segs, device), values(w, layer, segs, device)], dim=2)
 
 
 # ----------------------------------------------------------------------------- resident sets

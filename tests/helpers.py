@@ -37,12 +37,12 @@ def chunk_major_to_blocks(t: torch.Tensor) -> np.ndarray:
     return bits(t.permute(0, 2, 1, 3).reshape(S, Nb, C * 8))
 
 
-def device_tiles(w, layer, device="cuda", chunk=8, step=0):
+def device_tiles(w, layer, device="cuda", chunk=8):
     """The layer's full KV cache in tile layout on the device, bf16 [S][Nb][2][16][D]."""
     out = torch.empty((w.S, w.Nb, 2, 16, w.D), dtype=torch.bfloat16, device=device)
     for s0 in range(0, w.S, chunk):
         segs = list(range(s0, min(w.S, s0 + chunk)))
-        out[s0:s0 + len(segs)] = wl.kv_tiles(w, layer, segs, device=device, step=step)
+        out[s0:s0 + len(segs)] = wl.kv_tiles(w, layer, segs, device=device)
     return out
 
 
