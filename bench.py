@@ -63,6 +63,9 @@ def _args(argv=None):
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
     p.add_argument("--attn", choices=["cluster", "balanced"], default="cluster",
                    help="attention split: per-head thread-block clusters, or SM-balanced with a workspace")
+    p.add_argument("--scoring", choices=["tc", "exact"], default="tc",
+                   help="tc: tensor-core estimates + certified selection; exact: fixed-order fp32 scores of every "
+                        "block (both give the same tables and plans)")
     return p.parse_args(argv)
 
 
@@ -371,7 +374,7 @@ class Workbench:
     one synthetic layer, the pinned host tier, and the queries of every drift
     step.  reset() puts every layer back to the prior tables and pools."""
 
-    def __init__(self, w, R, dev, balanced_attn=False):
+    def __init__(self, w, R, dev, balanced_attn=False, scoring="tc"):
         import torch
 
         import sparse_kv_cache_quest_gb300 as okv
@@ -391,7 +394,7 @@ class Workbench:
         self.strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
         self.layers = []
         for _ in range(R):
-            lay = okv.DecodeLayer(shape, device=dev, balanced_attn=balanced_attn)
+            lay = okv.DecodeLayer(shape, device=dev, balanced_attn=balanced_attn, scoring=scoring)
             lay.build_summary(tiles, self.sl, 0, w.Nb, strides=self.strides)
             self.layers.append(lay)
         self.table0 = _gpu_prior(w, self.layers[0], self.sl, self.q[0]).to(dev)
@@ -445,15 +448,24 @@ def _kernel_times(wb, dev, n_rep=20):
     import torch
     w = wb.w
     q, qd, sl = wb.q[0], wb.qd[0], wb.sl
+    import sparse_kv_cache_quest_gb300 as okv
+    sh = wb.layers[0].shape
+
+    def exact_score(lay, st_):
+        okv.oasis_score_blocks(lay.kmin, lay.kmax, sh.Nb_max, qd, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D, sl, sh.W,
+                               lay.scores, lay.status, st_)
+
     calls = {"score": lambda lay, st_: lay.score(qd, sl, stream=st_),
              "attn": lambda lay, st_: lay.attend(q, sl, stream=st_),
-             "select": lambda lay, st_: lay.select(sl, stream=st_),
+             "select": lambda lay, st_: lay.select(sl, stream=st_, qdraft=qd),
              "stage": lambda lay, st_: lay.stage(wb.host, wb.seg_stride, w.Nb, stream=st_),
              "summary_update": lambda lay, st_: lay.build_summary(wb.new_keys, sl, blk_begin=w.Nb - 1, blk_count=1,
                                                                   stream=st_),
              # the full build at sparsification time (not part of a decode step): every block's keys
              "summary_full_build": lambda lay, st_: lay.build_summary(wb.tiles, sl, 0, w.Nb, strides=wb.strides,
                                                                       stream=st_)}
+    if wb.layers[0].scoring == "tc":
+        calls["score_exact"] = exact_score      # the fixed-order kernel alone, for comparison
     kern = {}
     n_launch = max(8, wb.R)
     for name, fn in calls.items():
@@ -476,7 +488,7 @@ def _kernel_times(wb, dev, n_rep=20):
     return kern
 
 
-def _roofline(w, kern):
+def _roofline(w, kern, scoring="tc"):
     peak, peak_kind = _peaks()
     fp32_peak = _fp32_peak_tfma()
     score_bytes = w.summary_bytes_per_layer()
@@ -485,30 +497,40 @@ def _roofline(w, kern):
     score_fma = w.S * w.nc * w.Nq * w.D
     k_gbs = {"score": score_bytes / (kern["score"] * 1e-6) / 1e9, "attn": attn_bytes / (kern["attn"] * 1e-6) / 1e9}
     dom = "attn" if kern["attn"] >= kern["score"] else "score"
-    kname = {"attn": "k_attn", "score": "k_score"}
+    kname = {"attn": "k_attn", "score": "k_score_tc" if scoring == "tc" else "k_score"}
+    sname = ("k_score_tc (oasis_score_blocks_tc, tensor cores)" if scoring == "tc"
+             else "k_score (oasis_score_blocks)")
     score_tfma = score_fma / (kern["score"] * 1e-6) / 1e12
-    # the scoring kernel is bound by whichever of its bytes and its FMAs takes longer at peak
-    score_alu_bound = score_fma / (fp32_peak * 1e12) > score_bytes / (peak * 1e9)
+    # the fixed-order kernel is bound by whichever of its bytes and its FMAs takes longer at peak;
+    # the tensor-core kernel by its bytes (its MMA work is a small fraction of the tensor roof)
+    score_alu_bound = scoring == "exact" and score_fma / (fp32_peak * 1e12) > score_bytes / (peak * 1e9)
     score_fp32 = {"achieved": score_tfma, "peak": fp32_peak, "unit": "TFMA/s", "frac": score_tfma / fp32_peak,
                   "algorithmic_fma_per_launch": score_fma,
                   "peak_kind": "nominal: 152 SMs x 128 FP32 lanes x 2,070 MHz (unit counts and maximum SM clock)",
                   "note": "the kernel issues two FMAs per term (one adds an exact zero), so it can reach at most 0.5"}
+    if scoring == "tc":
+        ex = kern.get("score_exact")
+        score_fp32 = None if ex is None else {
+            "kernel": "k_score (oasis_score_blocks, fixed-order fp32, for comparison)", "us": ex,
+            "achieved_tfma": score_fma / (ex * 1e-6) / 1e12, "peak_tfma": fp32_peak,
+            "frac": score_fma / (ex * 1e-6) / 1e12 / fp32_peak, "gbs": score_bytes / (ex * 1e-6) / 1e9}
     timing = "CUDA graph of back-to-back launches over the layers' buffer sets, CUDA events on the replay stream"
     pk = f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind
     if dom == "score" and score_alu_bound:
-        roof = {"kernel": "k_score (oasis_score_blocks)", "bound": "alu", **score_fp32,
+        roof = {"kernel": sname, "bound": "alu", **score_fp32,
                 "traffic": _traffic("k_score", w), "timing": timing,
                 "other": {"attn": {"us": kern["attn"], "gbs": k_gbs["attn"], "frac": k_gbs["attn"] / peak,
                                    "traffic": _traffic("k_attn", w)},
                           "score_hbm": {"gbs": k_gbs["score"], "frac": k_gbs["score"] / peak}}}
     else:
-        roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": "k_score (oasis_score_blocks)"}[dom],
+        roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": sname}[dom],
                 "bound": "hbm", "achieved": k_gbs[dom], "peak": peak, "unit": "GB/s", "frac": k_gbs[dom] / peak,
                 "peak_kind": pk, "traffic": _traffic(kname[dom], w),
                 "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes, "timing": timing,
                 "other": {k: {"us": kern[k], "gbs": k_gbs[k], "frac": k_gbs[k] / peak, "traffic": _traffic(kname[k], w)}
                           for k in k_gbs if k != dom}}
-        roof["other"]["score_fp32"] = score_fp32
+        if score_fp32 is not None:
+            roof["other"]["score_fixed_order" if scoring == "tc" else "score_fp32"] = score_fp32
     # full summary build: reads the keys of every block (16 tokens x D bf16), writes kmin and kmax
     build_bytes = w.S * w.Nb * (16 * w.D * 2 + 2 * w.D * 2)
     build_gbs = build_bytes / (kern["summary_full_build"] * 1e-6) / 1e9
@@ -543,7 +565,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # ---- setup (untimed): KV cache, summaries, prior tables, pools, pinned host tier
-    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced")
+    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring)
     graphs = wb.graphs(args)
     wb.reset()                                  # the capture's warm-up ran one step: start from the prior again
 
@@ -596,6 +618,7 @@ def run_ours(args):
                     "staging_streams": args.xf_streams,
                     "foreground_priority": args.fg_priority,
                     "attention_split": args.attn,
+                    "scoring": args.scoring,
                     "step": f"one decode step: the whole path (summary update, scoring, capped selection, staging, "
                             f"attention) over each of the {R} layers, layer-pipelined in one CUDA graph; tables "
                             f"advance from step to step, step i uses the queries of drift step i mod "
@@ -608,7 +631,7 @@ def run_ours(args):
                 "gpu_launches": 5 * R * K,
                 "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
         if kern is not None:
-            line["roofline"] = _roofline(w, kern)
+            line["roofline"] = _roofline(w, kern, args.scoring)
             line["kernels_us"] = kern
         print(json.dumps(line), flush=True)
     if world > 1:

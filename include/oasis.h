@@ -146,6 +146,32 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
                        float *scores, int32_t *status, oasis_stream_t stream);
 
 /*
+ * The same look-ahead scores on the tensor cores, each with a certified error
+ * radius ([XR] §3 decode flow; §4 Fig. 7).  Per segment the scan is a dense
+ * product of the candidate blocks' summaries [kmax | kmin] (2D values per
+ * block) with the head's split queries [q+ ; q-] (q+ = q where q >= 0, q- =
+ * q where q < 0, +0 elsewhere), run as tcgen05 MMAs with fp32 accumulation;
+ * the block score is the max over the query columns.
+ *
+ * scores[s][b] = s~, radius[s][b] = r (both float32 [S][Nb_max]), written
+ * for the same candidate blocks as oasis_score_blocks, such that the score s
+ * that oasis_score_blocks computes for the block satisfies |s~ - s| <= r.
+ *   r = 2^-12 (|s~| + 2 C) + 2^-110,  C = sum_d Q_d c_d,
+ * Q_d = max over the head's query vectors of |q_d|, c_d = |kmax_d| where
+ * kmax_d < 0, kmin_d where kmin_d > 0, else 0.  The sum of the absolute terms
+ * of any query is at most |s~| + 2C (up to rounding), and both the fixed-order
+ * fp32 sum and the tensor cores' fp32 accumulation of 2D terms stay within
+ * 2^-16 of it, so r carries a margin of 16.  A NaN score gets radius +inf.
+ * oasis_select_topk_capped_tc turns these into the exact selection.
+ * Host-side checks, alignment and EINVAL cases: as oasis_score_blocks, plus
+ * radius (4-byte aligned, not NULL).  One CTA per SM with about 200 KB of
+ * shared memory; every internal wait is bounded (OASIS_STATUS_TIMEOUT).
+ */
+int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
+                          int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
+                          float *scores, float *radius, int32_t *status, oasis_stream_t stream);
+
+/*
  * Per-KV-head top-K with capped admission ([XR] §3 decode flow and component
  * table "Capped Eviction Policy" and "Head-wise Mapping"; §4 innovations;
  * [LP] FAQ Q7).  One segment, nc = ceil(seq_len/16) - W candidates:
@@ -170,6 +196,35 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
 int oasis_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                              int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                              oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, oasis_stream_t stream);
+
+/*
+ * The same selection from tensor-core estimates (oasis_score_blocks_tc): the
+ * outputs table_out, plan and plan_count are exactly those that
+ * oasis_select_topk_capped gives on the fixed-order scores of
+ * oasis_score_blocks ([XR] §3 decode flow, component table "Capped Eviction
+ * Policy"; the certification is this library's own).
+ * Each of the rule's three decisions splits a set into its first m members
+ * and the rest: T (the first K candidates), A (the first cap of T \ R) and
+ * the evicted (the last max(0, |A| - empty slots) of R \ T).  With the
+ * intervals [s~ - r, s~ + r], a member whose interval lies above every
+ * interval of the members ranked after the first m by the estimates (or below
+ * every interval of the first m) is settled; every other member's score is
+ * recomputed with the oasis_score_blocks arithmetic from kmin, kmax and
+ * qdraft, and the selection runs on the mixed scores.
+ * scores:  in: the estimates s~ [S][Nb_max]; out: the recomputed blocks hold
+ *          their fixed-order scores, the others keep their estimates.
+ * radius:  [S][Nb_max], any r with |s~ - s| <= r (a larger r only means more
+ *          recomputation; +inf recomputes every candidate).
+ * kmin, kmax, qdraft, G, Nd, D: as for oasis_score_blocks.
+ * Other arguments, outputs and status bits: as oasis_select_topk_capped.
+ * EINVAL: as oasis_select_topk_capped, or a NULL or misaligned summary / query
+ * / radius pointer, D not 64 or 128, G not in [1, 16], Nd < 1, G*Nd > 64,
+ * Nb_max > 16384, or shared memory beyond 200 KB for the shape.
+ */
+int oasis_select_topk_capped_tc(float *scores, const float *radius, const uint16_t *kmin, const uint16_t *kmax,
+                                const uint16_t *qdraft, int G, int Nd, int D, int Nb_max, const int32_t *seq_len,
+                                int B, int Hkv, int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
+                                oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, oasis_stream_t stream);
 
 /*
  * Carry out the transfer plan: copy each planned block's KV tile from the host

@@ -22,8 +22,8 @@ STATUS_TABLE_RANGE, STATUS_TABLE_DUP, STATUS_NAN_SCORE = 1, 2, 4
 STATUS_PLAN_RANGE, STATUS_SEQ_LEN, STATUS_TIMEOUT = 8, 16, 32
 
 EXPORTS = (
-    "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks",
-    "oasis_select_topk_capped", "oasis_stage_blocks", "oasis_sparse_decode_attn",
+    "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks", "oasis_score_blocks_tc",
+    "oasis_select_topk_capped", "oasis_select_topk_capped_tc", "oasis_stage_blocks", "oasis_sparse_decode_attn",
     "oasis_attn_workspace_bytes", "oasis_sparse_decode_attn_ws", "oasis_sparse_decode_attn_noalloc",
 )
 
@@ -50,7 +50,10 @@ _SIGS = {
     "oasis_abi_version": (_I, []),
     "oasis_build_summary": (_I, [_P, _I64, _I64, _I64, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _P]),
     "oasis_score_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "oasis_score_blocks_tc": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "oasis_select_topk_capped": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "oasis_select_topk_capped_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
+                                        _P]),
     "oasis_stage_blocks": (_I, [_P, _I64, _I, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P]),
     "oasis_sparse_decode_attn": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
     "oasis_attn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
@@ -124,11 +127,25 @@ def oasis_score_blocks(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W,
         _ptr(status), _stream(stream)))
 
 
+def oasis_score_blocks_tc(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, radius, status=None,
+                          stream=None):
+    return _check("oasis_score_blocks_tc", load().oasis_score_blocks_tc(
+        _ptr(kmin), _ptr(kmax), Nb_max, _ptr(qdraft), B, Hkv, G, Nd, D, _ptr(seq_len), W, _ptr(scores),
+        _ptr(radius), _ptr(status), _stream(stream)))
+
+
 def oasis_select_topk_capped(scores, Nb_max, seq_len, B, Hkv, K, W, cap, table_in, table_out, plan,
                              plan_count, status, stream=None):
     return _check("oasis_select_topk_capped", load().oasis_select_topk_capped(
         _ptr(scores), Nb_max, _ptr(seq_len), B, Hkv, K, W, cap, _ptr(table_in), _ptr(table_out), _ptr(plan),
         _ptr(plan_count), _ptr(status), _stream(stream)))
+
+
+def oasis_select_topk_capped_tc(scores, radius, kmin, kmax, qdraft, G, Nd, D, Nb_max, seq_len, B, Hkv, K, W, cap,
+                                table_in, table_out, plan, plan_count, status, stream=None):
+    return _check("oasis_select_topk_capped_tc", load().oasis_select_topk_capped_tc(
+        _ptr(scores), _ptr(radius), _ptr(kmin), _ptr(kmax), _ptr(qdraft), G, Nd, D, Nb_max, _ptr(seq_len), B, Hkv,
+        K, W, cap, _ptr(table_in), _ptr(table_out), _ptr(plan), _ptr(plan_count), _ptr(status), _stream(stream)))
 
 
 def oasis_stage_blocks(host_kv, host_seg_stride_bytes, host_nb, plan, plan_count, cap, B, Hkv, D, pool,

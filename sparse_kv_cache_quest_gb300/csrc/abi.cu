@@ -137,6 +137,20 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
                                            status, stream));
 }
 
+int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
+                          int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W, float *scores,
+                          float *radius, int32_t *status, oasis_stream_t stream) {
+  if (!kmin || !kmax || !qdraft || !seq_len || !scores || !radius) return OASIS_EINVAL;
+  if (!d_ok(D) || !segs_ok(B, Hkv) || Nb_max < 1 || W < 0) return OASIS_EINVAL;
+  if (G < 1 || G > 16 || Nd < 1 || G * Nd > 64) return OASIS_EINVAL;
+  if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(qdraft) || !aligned4(seq_len) || !aligned4(scores) ||
+      !aligned4(radius))
+    return OASIS_EINVAL;
+  if (status && !aligned4(status)) return OASIS_EINVAL;
+  return finish(oasis::launch_score_blocks_tc(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores,
+                                              radius, status, stream));
+}
+
 int oasis_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv, int K,
                              int W, int cap, const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
                              int32_t *plan_count, int32_t *status, oasis_stream_t stream) {
@@ -148,6 +162,25 @@ int oasis_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq
     return OASIS_EINVAL;
   return finish(oasis::launch_select_topk_capped(scores, Nb_max, seq_len, B, Hkv, K, W, cap, table_in, table_out,
                                                  plan, plan_count, status, stream));
+}
+
+int oasis_select_topk_capped_tc(float *scores, const float *radius, const uint16_t *kmin, const uint16_t *kmax,
+                                const uint16_t *qdraft, int G, int Nd, int D, int Nb_max, const int32_t *seq_len,
+                                int B, int Hkv, int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
+                                oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, oasis_stream_t stream) {
+  if (!scores || !radius || !kmin || !kmax || !qdraft || !seq_len || !table_in || !table_out || !plan ||
+      !plan_count || !status)
+    return OASIS_EINVAL;
+  if (!segs_ok(B, Hkv) || K < 1 || K > 1024 || W < 0 || W > 256 || cap < 0 || cap > K) return OASIS_EINVAL;
+  if (Nb_max < 1 || Nb_max > 16384 || !d_ok(D) || G < 1 || G > 16 || Nd < 1 || G * Nd > 64) return OASIS_EINVAL;
+  if (!aligned4(scores) || !aligned4(radius) || !aligned16(kmin) || !aligned16(kmax) || !aligned16(qdraft) ||
+      !aligned4(seq_len) || !aligned4(table_in) || !aligned4(table_out) || !aligned4(plan) || !aligned4(plan_count) ||
+      !aligned4(status))
+    return OASIS_EINVAL;
+  if (oasis::select_tc_smem_bytes(Nb_max, K, W, cap, D, G * Nd) > 200 * 1024) return OASIS_EINVAL;
+  return finish(oasis::launch_select_topk_capped_tc(scores, radius, kmin, kmax, qdraft, G, Nd, D, Nb_max, seq_len,
+                                                    B, Hkv, K, W, cap, table_in, table_out, plan, plan_count, status,
+                                                    stream));
 }
 
 int oasis_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int host_nb, const oasis_xfer_t *plan,

@@ -132,9 +132,18 @@ cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t 
 cudaError_t launch_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
                                 int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
                                 float *scores, int32_t *status, cudaStream_t st);
+cudaError_t launch_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
+                                   int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
+                                   float *scores, float *radius, int32_t *status, cudaStream_t st);
 cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                                       oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st);
+size_t select_tc_smem_bytes(int Nb_max, int K, int W, int cap, int D, int Nq);
+cudaError_t launch_select_topk_capped_tc(float *scores, const float *radius, const uint16_t *kmin,
+                                         const uint16_t *kmax, const uint16_t *qdraft, int G, int Nd, int D,
+                                         int Nb_max, const int32_t *seq_len, int B, int Hkv, int K, int W, int cap,
+                                         const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
+                                         int32_t *plan_count, int32_t *status, cudaStream_t st);
 cudaError_t launch_stage_blocks(const void *host_kv, int64_t host_seg_stride_bytes, int host_nb,
                                 const oasis_xfer_t *plan, const int32_t *plan_count, int cap, int B, int Hkv,
                                 int D, uint16_t *pool, int slots_per_seg, int32_t *status, cudaStream_t st);

@@ -89,77 +89,15 @@ struct SelScalars {
 
 static_assert(sizeof(SelScalars) + 3 * 256 * sizeof(uint32_t) <= kStaticSmemBound, "static shared memory bound");
 
-__global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ scores, int Nb_max,
-                                                     const int32_t *__restrict__ seq_len, int Hkv, int K, int W,
-                                                     int cap, const int32_t *table_in, int32_t *table_out,
-                                                     oasis_xfer_t *__restrict__ plan, int32_t *__restrict__ plan_count,
-                                                     int32_t *status) {
-  extern __shared__ __align__(16) unsigned char smraw[];
-  __shared__ SelScalars sc;
-  __shared__ __align__(16) uint32_t hist[3][256];  // pass p counts into hist[p % 3], clears hist[(p + 1) % 3]
-
-  const int s = blockIdx.x;
+// T as a bitmap: the first min(K, nc) candidates by (key desc, block asc).
+// 4-pass 8-bit MSB radix select of the K-th largest key (warp-aggregated
+// shared-memory histograms, triple-buffered so each pass takes one barrier),
+// then the keys equal to it taken in ascending block order through a
+// block-wide prefix count.  bmT must be clear; all threads call it; the caller
+// synchronises before reading bmT.
+__device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, uint32_t (*hist)[256],
+                            SelScalars &sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slots = K + W;
-  const int words = (Nb_max + 31) >> 5;
-
-  uint64_t *listN = reinterpret_cast<uint64_t *>(smraw);       // [K]
-  uint64_t *listE = listN + K;                                 // [K]
-  uint32_t *keys = reinterpret_cast<uint32_t *>(listE + K);   // [Nb_max]
-  uint32_t *bmR = keys + Nb_max;                               // [words]
-  uint32_t *bmT = bmR + words;                                 // [words]
-  int32_t *tin = reinterpret_cast<int32_t *>(bmT + words);     // [slots]
-  int32_t *slotE = tin + slots;                                // [K]
-  int32_t *rankN = slotE + K;                                  // [K]
-  int32_t *aSorted = rankN + K;                                // [cap]
-  int32_t *fList = aSorted + cap;                              // [cap]
-  int32_t *fSorted = fList + cap;                              // [cap]
-
-  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status, tid == 0 && (s % Hkv) == 0);
-  const int nc = max(0, ceil_div(L, kBlockTokens) - W);
-
-  // 1. table, bitmaps, keys
-  for (int i = tid; i < slots; i += kThreads) tin[i] = table_in[static_cast<int64_t>(s) * slots + i];
-  for (int i = tid; i < words; i += kThreads) {
-    bmR[i] = 0u;
-    bmT[i] = 0u;
-  }
-  if (tid == 0) {
-    sc.err = 0;
-    sc.nN = sc.nE = sc.nF = sc.nEmpty = 0;
-  }
-  for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
-  bool nan = false;
-  const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
-  for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
-  __syncthreads();
-  if (nan) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
-
-  // 2. residents: range and duplicate checks, R bitmap, empty count
-  for (int i = tid; i < K; i += kThreads) {
-    const int blk = tin[i];
-    if (blk == -1) {
-      atomicAdd(&sc.nEmpty, 1);
-    } else if (blk < 0 || blk >= nc) {
-      atomicOr(&sc.err, OASIS_STATUS_TABLE_RANGE);
-    } else {
-      const uint32_t m = 1u << (blk & 31);
-      if (atomicOr(&bmR[blk >> 5], m) & m) atomicOr(&sc.err, OASIS_STATUS_TABLE_DUP);
-    }
-  }
-  __syncthreads();
-  const int err = sc.err;
-  if (err & (OASIS_STATUS_TABLE_RANGE | OASIS_STATUS_TABLE_DUP)) {
-    for (int i = tid; i < slots; i += kThreads) table_out[static_cast<int64_t>(s) * slots + i] = tin[i];
-    for (int k = tid; k < cap; k += kThreads) plan[static_cast<int64_t>(s) * cap + k] = oasis_xfer_t{-1, -1};
-    if (tid == 0) {
-      plan_count[s] = 0;
-      report(status, err);
-    }
-    return;
-  }
-
-  // 3. T = top-K candidates
   if (nc <= K) {
     for (int b = tid; b < nc; b += kThreads) atomicOr(&bmT[b >> 5], 1u << (b & 31));
   } else {
@@ -238,6 +176,250 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
       if (in) atomicOr(&bmT[b >> 5], 1u << (b & 31));
     }
   }
+}
+
+
+// ---- certified selection from tensor-core score estimates ------------------
+// The certified kernel receives for every candidate an estimate s~ and a
+// radius r with |s~ - s| <= r around the fixed-order score s.  A selection
+// decision that splits a set into its first m members and the rest (T: the
+// first K candidates; A: the first cap of T \ R; the evicted: the last nEvict
+// of R \ T) is settled without s wherever the intervals separate: with X~ the
+// first m by the estimates, lo = min over X~ of (s~ - r) and hi = max over the
+// rest of (s~ + r), a member with s~ - r > hi is in the first m whatever the
+// exact order (at most m - 1 others can rank above it), one with s~ + r < lo is
+// not (m others surely rank above it).  Every other member is recomputed with
+// the fixed-order arithmetic, and the selection then runs on the mixed scores:
+// the settled members keep their side, the recomputed ones are ordered
+// exactly, so every set equals the one the exact scores give.
+constexpr int kBatch = 32;  // blocks recomputed per pass
+
+struct CertArgs {
+  float *scores;  // in: estimates; out: the recomputed blocks' fixed-order scores
+  const float *radius;
+  const uint16_t *kmin, *kmax, *qdraft;
+  int G, Nd;
+};
+
+__device__ float block_reduce(float v, bool is_max, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    v = is_max ? fmaxf(v, y) : fminf(v, y);
+  }
+  __syncthreads();  // red may still be read by a previous reduction
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, red[w]) : fminf(r, red[w]);
+  return r;
+}
+
+// Fixed-order fp32 scores of the listed blocks (the oasis_score_blocks
+// arithmetic: per query, sum over d ascending from +0 of q_d * (q_d >= 0 ?
+// kmax_d : kmin_d), one rounding per term; max over the queries, NaN kept).
+// Writes them to srow and their keys to keys, marks them in bmX.
+template <int CH>
+__device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
+                                 int Nq, const float *qsm, uint4 *stage, float *res, float *srow, uint32_t *keys,
+                                 uint32_t *bmX, SelScalars &sc) {
+  constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
+  const int tid = threadIdx.x;
+  for (int e0 = 0; e0 < n; e0 += kBatch) {
+    const int nb = min(kBatch, n - e0);
+    for (int i = tid; i < nb * 2 * CH; i += kThreads) {
+      const int e = i / (2 * CH), k = i % (2 * CH), c = k % CH;
+      const int b = xl[e0 + e];
+      stage[e * ES + k] = __ldg((k < CH ? gmin : gmax) + static_cast<int64_t>(c) * Nb_max + b);
+    }
+    __syncthreads();
+    for (int i = tid; i < nb * Nq; i += kThreads) {
+      const int e = i / Nq, j = i % Nq;
+      const uint4 *st = stage + e * ES;
+      float acc = 0.0f;
+#pragma unroll 2
+      for (int c = 0; c < CH; ++c) {
+        const uint4 mn = st[c], mx = st[CH + c];
+        const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w}, wx[4] = {mx.x, mx.y, mx.z, mx.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float q = qsm[(c * 8 + t) * Nq + j];
+          const uint32_t w = q >= 0.0f ? wx[t >> 1] : wn[t >> 1];
+          acc = fmaf(q, (t & 1) ? bf16_hi(w) : bf16_lo(w), acc);  // exact product, one rounding
+        }
+      }
+      res[e * Nq + j] = acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < nb; e += kThreads) {
+      float best = -INFINITY;
+      bool nan = false;
+      for (int j = 0; j < Nq; ++j) {
+        const float v = res[e * Nq + j];
+        nan |= v != v;
+        best = fmaxf(best, v);
+      }
+      const float v = nan ? __uint_as_float(0x7FC00000u) : best;
+      const int b = xl[e0 + e];
+      srow[b] = v;
+      bool isn = false;
+      keys[b] = score_key(v, isn);
+      if (isn) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
+      atomicOr(&bmX[b >> 5], 1u << (b & 31));
+    }
+    __syncthreads();
+  }
+}
+
+// interval of block b: recomputed blocks are exact (radius 0)
+__device__ __forceinline__ void interval(const float *srow, const float *rrow, const uint32_t *bmX, int b, float &lo,
+                                         float &hi) {
+  const float v = srow[b];
+  const float r = bit(bmX, b) ? 0.0f : rrow[b];
+  lo = v - r;
+  hi = v + r;
+}
+
+// CERTIFY = false: the selection on exact scores.  CERTIFY = true: `scores`
+// holds estimates with radii (CertArgs); the decisions the estimates cannot
+// settle are settled by recomputing fixed-order scores (see above).
+template <bool CERTIFY, int CH>
+__global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb_max,
+                                                     const int32_t *__restrict__ seq_len, int Hkv, int K, int W,
+                                                     int cap, const int32_t *table_in, int32_t *table_out,
+                                                     oasis_xfer_t *__restrict__ plan, int32_t *__restrict__ plan_count,
+                                                     int32_t *status, CertArgs ca) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  __shared__ SelScalars sc;
+  __shared__ __align__(16) uint32_t hist[3][256];  // pass p counts into hist[p % 3], clears hist[(p + 1) % 3]
+  __shared__ float red[kWarps];
+  __shared__ int nX;
+
+  const int s = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slots = K + W;
+  const int words = (Nb_max + 31) >> 5;
+
+  uint64_t *listN = reinterpret_cast<uint64_t *>(smraw);       // [K]
+  uint64_t *listE = listN + K;                                 // [K]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(listE + K);   // [Nb_max]
+  uint32_t *bmR = keys + Nb_max;                               // [words]
+  uint32_t *bmT = bmR + words;                                 // [words]
+  int32_t *tin = reinterpret_cast<int32_t *>(bmT + words);     // [slots]
+  int32_t *slotE = tin + slots;                                // [K]
+  int32_t *rankN = slotE + K;                                  // [K]
+  int32_t *aSorted = rankN + K;                                // [cap]
+  int32_t *fList = aSorted + cap;                              // [cap]
+  int32_t *fSorted = fList + cap;                              // [cap]
+  // certified selection only (sized by cert_smem_bytes)
+  constexpr int D = CH * 8;
+  const int Nq = CERTIFY ? ca.G * ca.Nd : 0;
+  unsigned char *craw = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(fSorted + cap) + 15) & ~static_cast<uintptr_t>(15));
+  uint4 *stage = reinterpret_cast<uint4 *>(craw);                  // [kBatch][2*CH + 1]
+  float *qsm = reinterpret_cast<float *>(stage + kBatch * (2 * CH + 1));  // [D][Nq]
+  float *res = qsm + D * Nq;                                       // [kBatch][Nq]
+  uint32_t *bmX = reinterpret_cast<uint32_t *>(res + kBatch * Nq); // [words] recomputed blocks
+  int32_t *xl = reinterpret_cast<int32_t *>(bmX + words);          // [Nb_max] blocks to recompute
+  int32_t *rankE = xl + Nb_max;                                    // [K]
+  float *srow_w = CERTIFY ? ca.scores + static_cast<int64_t>(s) * Nb_max : nullptr;
+  const float *rrow = CERTIFY ? ca.radius + static_cast<int64_t>(s) * Nb_max : nullptr;
+  const uint4 *gmin = CERTIFY ? reinterpret_cast<const uint4 *>(ca.kmin) + static_cast<int64_t>(s) * CH * Nb_max
+                              : nullptr;
+  const uint4 *gmax = CERTIFY ? reinterpret_cast<const uint4 *>(ca.kmax) + static_cast<int64_t>(s) * CH * Nb_max
+                              : nullptr;
+
+  const int L = load_len(seq_len, s / Hkv, Nb_max * kBlockTokens, status, tid == 0 && (s % Hkv) == 0);
+  const int nc = max(0, ceil_div(L, kBlockTokens) - W);
+
+  // 1. table, bitmaps, keys
+  for (int i = tid; i < slots; i += kThreads) tin[i] = table_in[static_cast<int64_t>(s) * slots + i];
+  for (int i = tid; i < words; i += kThreads) {
+    bmR[i] = 0u;
+    bmT[i] = 0u;
+  }
+  if (tid == 0) {
+    sc.err = 0;
+    sc.nN = sc.nE = sc.nF = sc.nEmpty = 0;
+  }
+  for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
+  if constexpr (CERTIFY) {
+    for (int i = tid; i < words; i += kThreads) bmX[i] = 0u;
+    // the segment's query vectors, widened: qsm[d][j], j = draft * G + head in group
+    const int Hq = Hkv * ca.G, bseq = s / Hkv, h = s % Hkv;
+    for (int i = tid; i < Nq * CH; i += kThreads) {
+      const int j = i / CH, c = i % CH, jd = j / ca.G, g = j % ca.G;
+      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+          ca.qdraft + ((static_cast<int64_t>(bseq) * ca.Nd + jd) * Hq + h * ca.G + g) * D + c * 8));
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int t = 0; t < 8; ++t) qsm[(c * 8 + t) * Nq + j] = (t & 1) ? bf16_hi(w4[t >> 1]) : bf16_lo(w4[t >> 1]);
+    }
+  }
+  bool nan = false;
+  const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
+  for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
+  __syncthreads();
+  if (nan) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
+
+  // 2. residents: range and duplicate checks, R bitmap, empty count
+  for (int i = tid; i < K; i += kThreads) {
+    const int blk = tin[i];
+    if (blk == -1) {
+      atomicAdd(&sc.nEmpty, 1);
+    } else if (blk < 0 || blk >= nc) {
+      atomicOr(&sc.err, OASIS_STATUS_TABLE_RANGE);
+    } else {
+      const uint32_t m = 1u << (blk & 31);
+      if (atomicOr(&bmR[blk >> 5], m) & m) atomicOr(&sc.err, OASIS_STATUS_TABLE_DUP);
+    }
+  }
+  __syncthreads();
+  const int err = sc.err;
+  if (err & (OASIS_STATUS_TABLE_RANGE | OASIS_STATUS_TABLE_DUP)) {
+    for (int i = tid; i < slots; i += kThreads) table_out[static_cast<int64_t>(s) * slots + i] = tin[i];
+    for (int k = tid; k < cap; k += kThreads) plan[static_cast<int64_t>(s) * cap + k] = oasis_xfer_t{-1, -1};
+    if (tid == 0) {
+      plan_count[s] = 0;
+      report(status, err);
+    }
+    return;
+  }
+
+  // 3. T = top-K candidates
+  if constexpr (CERTIFY) {
+    if (nc > K) {
+      // T by the estimates, then the blocks it cannot settle
+      topk_bitmap(keys, nc, K, bmT, hist, sc);
+      __syncthreads();
+      float lo_in = INFINITY, hi_out = -INFINITY;
+      for (int b = tid; b < nc; b += kThreads) {
+        float lo, hi;
+        interval(srow, rrow, bmX, b, lo, hi);
+        if (lo != lo || hi != hi) continue;  // NaN estimate: recomputed below
+        if (bit(bmT, b))
+          lo_in = fminf(lo_in, lo);
+        else
+          hi_out = fmaxf(hi_out, hi);
+      }
+      lo_in = block_reduce(lo_in, false, red);
+      hi_out = block_reduce(hi_out, true, red);
+      if (tid == 0) nX = 0;
+      __syncthreads();
+      for (int b = tid; b < nc; b += kThreads) {
+        float lo, hi;
+        interval(srow, rrow, bmX, b, lo, hi);
+        if (!(lo > hi_out) && !(hi < lo_in)) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
+      }
+      __syncthreads();
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, bmX, sc);
+      for (int i = tid; i < words; i += kThreads) bmT[i] = 0u;
+      for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
+      __syncthreads();
+    }
+  }
+  topk_bitmap(keys, nc, K, bmT, hist, sc);
   __syncthreads();
 
   // 4. lists: N = T \ R (candidates to admit), E = R \ T (residents that may go)
@@ -262,6 +444,79 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *__restrict__ s
   const int nA = min(cap, nN);
   const int nEvict = max(0, nA - nEmpty);
   const int nFill = nA - nEvict;
+
+  if constexpr (CERTIFY) {
+    // A = the first nA of N, evicted = the last nEvict of E: settle both by the
+    // estimates' intervals, recompute what they cannot settle
+    const bool certA = nN > nA, certE = nEvict > 0 && nE > nEvict;
+    if (certA || certE) {
+      for (int i = warp; i < nN; i += kWarps) {  // rank by the estimates (larger first)
+        const uint64_t ci = listN[i];
+        int r = 0;
+        for (int j0 = 0; j0 < nN; j0 += 32) {
+          const int j = j0 + lane;
+          r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && listN[j] > ci));
+        }
+        if (lane == 0) rankN[i] = r;
+      }
+      for (int i = warp; i < nE; i += kWarps) {  // rank from the bottom (smaller first)
+        const uint64_t ci = listE[i];
+        int r = 0;
+        for (int j0 = 0; j0 < nE; j0 += 32) {
+          const int j = j0 + lane;
+          r += __popc(__ballot_sync(0xFFFFFFFFu, j < nE && listE[j] < ci));
+        }
+        if (lane == 0) rankE[i] = r;
+      }
+      __syncthreads();
+      float a_lo = INFINITY, a_hi = -INFINITY, e_lo = INFINITY, e_hi = -INFINITY;
+      for (int i = tid; i < nN; i += kThreads) {
+        float lo, hi;
+        interval(srow, rrow, bmX, composite_block(listN[i]), lo, hi);
+        if (rankN[i] < nA)
+          a_lo = fminf(a_lo, lo);
+        else
+          a_hi = fmaxf(a_hi, hi);
+      }
+      for (int i = tid; i < nE; i += kThreads) {
+        float lo, hi;
+        interval(srow, rrow, bmX, composite_block(listE[i]), lo, hi);
+        if (rankE[i] < nEvict)
+          e_hi = fmaxf(e_hi, hi);  // evicted by the estimates
+        else
+          e_lo = fminf(e_lo, lo);  // kept by the estimates
+      }
+      a_lo = block_reduce(a_lo, false, red);
+      a_hi = block_reduce(a_hi, true, red);
+      e_lo = block_reduce(e_lo, false, red);
+      e_hi = block_reduce(e_hi, true, red);
+      if (tid == 0) nX = 0;
+      __syncthreads();
+      for (int i = tid; i < nN && certA; i += kThreads) {
+        const int b = composite_block(listN[i]);
+        float lo, hi;
+        interval(srow, rrow, bmX, b, lo, hi);
+        if (!bit(bmX, b) && !(lo > a_hi) && !(hi < a_lo)) xl[atomicAdd(&nX, 1)] = b;
+      }
+      for (int i = tid; i < nE && certE; i += kThreads) {
+        const int b = composite_block(listE[i]);
+        float lo, hi;
+        interval(srow, rrow, bmX, b, lo, hi);
+        if (!bit(bmX, b) && !(lo > e_hi) && !(hi < e_lo)) xl[atomicAdd(&nX, 1)] = b;
+      }
+      __syncthreads();
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, bmX, sc);
+      for (int i = tid; i < nN; i += kThreads) {
+        const int b = composite_block(listN[i]);
+        listN[i] = composite(keys[b], b);
+      }
+      for (int i = tid; i < nE; i += kThreads) {
+        const int b = composite_block(listE[i]);
+        listE[i] = composite(keys[b], b);
+      }
+      __syncthreads();
+    }
+  }
 
   // 5. A = the nA best of N; freed slots = first nFill empty slots + the nEvict worst of E.
   // Every rank is a count over a list of at most K entries: one warp per entry,
@@ -343,6 +598,14 @@ size_t select_smem_bytes(int Nb_max, int K, int W, int cap) {
          sizeof(int32_t) * (static_cast<size_t>(K + W) + 2 * K + 3 * static_cast<size_t>(cap));
 }
 
+// the certified kernel's extra shared memory (after the above, 16-byte aligned)
+size_t cert_smem_bytes(int Nb_max, int K, int D, int Nq) {
+  const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
+  const size_t CH = static_cast<size_t>(D) / 8;
+  return 16 + sizeof(uint4) * kBatch * (2 * CH + 1) + sizeof(float) * (static_cast<size_t>(D) * Nq + kBatch * Nq) +
+         sizeof(uint32_t) * words + sizeof(int32_t) * (static_cast<size_t>(Nb_max) + K);
+}
+
 cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                                       oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st) {
@@ -350,12 +613,37 @@ cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int
   // static (histograms, scalars) + dynamic shared memory may pass the 48 KiB
   // default before the dynamic part alone does
   if (smem + kStaticSmemBound > 48 * 1024) {
-    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select), smem);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select<false, 1>), smem);
     if (e != cudaSuccess) return e;
   }
   LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);
-  return cudaLaunchKernelEx(&lc.cfg, k_select, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in, table_out, plan,
-                            plan_count, status);
+  return cudaLaunchKernelEx(&lc.cfg, k_select<false, 1>, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in,
+                            table_out, plan, plan_count, status, CertArgs{});
+}
+
+size_t select_tc_smem_bytes(int Nb_max, int K, int W, int cap, int D, int Nq) {
+  return select_smem_bytes(Nb_max, K, W, cap) + cert_smem_bytes(Nb_max, K, D, Nq);
+}
+
+cudaError_t launch_select_topk_capped_tc(float *scores, const float *radius, const uint16_t *kmin,
+                                         const uint16_t *kmax, const uint16_t *qdraft, int G, int Nd, int D,
+                                         int Nb_max, const int32_t *seq_len, int B, int Hkv, int K, int W, int cap,
+                                         const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
+                                         int32_t *plan_count, int32_t *status, cudaStream_t st) {
+  const size_t smem = select_tc_smem_bytes(Nb_max, K, W, cap, D, G * Nd);
+  const void *fn = D == 128 ? reinterpret_cast<const void *>(k_select<true, 16>)
+                            : reinterpret_cast<const void *>(k_select<true, 8>);
+  if (smem + kStaticSmemBound > 48 * 1024) {
+    cudaError_t e = raise_smem_limit(fn, smem);
+    if (e != cudaSuccess) return e;
+  }
+  const CertArgs ca{scores, radius, kmin, kmax, qdraft, G, Nd};
+  LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);
+  if (D == 128)
+    return cudaLaunchKernelEx(&lc.cfg, k_select<true, 16>, static_cast<const float *>(scores), Nb_max, seq_len, Hkv,
+                              K, W, cap, table_in, table_out, plan, plan_count, status, ca);
+  return cudaLaunchKernelEx(&lc.cfg, k_select<true, 8>, static_cast<const float *>(scores), Nb_max, seq_len, Hkv, K,
+                            W, cap, table_in, table_out, plan, plan_count, status, ca);
 }
 
 }  // namespace oasis

@@ -55,9 +55,15 @@ class DecodeLayer:
 
     balanced_attn: run the attention as the SM-balanced split with a workspace
     of this layer's own (oasis_sparse_decode_attn_ws) instead of the per-head
-    cluster split (oasis_sparse_decode_attn)."""
+    cluster split (oasis_sparse_decode_attn).
+    scoring: "exact" - every score in the fixed-order fp32 arithmetic
+    (oasis_score_blocks, then oasis_select_topk_capped); "tc" - tensor-core
+    estimates with radii (oasis_score_blocks_tc), then the certified selection
+    (oasis_select_topk_capped_tc), which recomputes the fixed-order scores the
+    decisions need.  Both give the same tables and plans; with "tc" the scores
+    buffer holds fixed-order values only for the recomputed blocks."""
 
-    def __init__(self, shape: LayerShape, device="cuda", balanced_attn: bool = False):
+    def __init__(self, shape: LayerShape, device="cuda", balanced_attn: bool = False, scoring: str = "exact"):
         self.shape = sh = shape
         dev = torch.device(device)
         self.device = dev
@@ -74,6 +80,11 @@ class DecodeLayer:
         self.lse = torch.zeros((sh.B, sh.Hq), dtype=torch.float32, device=dev)
         self.scale = 1.0 / math.sqrt(sh.D)
         self.attn_ws = ob.attn_workspace(sh.B, sh.Hkv, sh.G, sh.D, sh.slots, device=dev) if balanced_attn else None
+        if scoring not in ("exact", "tc"):
+            raise ValueError(f"scoring must be 'exact' or 'tc', not {scoring!r}")
+        self.scoring = scoring
+        self.radius = torch.zeros_like(self.scores) if scoring == "tc" else None
+        self._qdraft = None                   # the drafts the last score() call read (the tc selection rereads them)
 
     # -- individual steps ---------------------------------------------------
     def build_summary(self, keys, seq_len, blk_begin=0, blk_count=None, strides=None, stream=None):
@@ -90,11 +101,26 @@ class DecodeLayer:
 
     def score(self, qdraft, seq_len, stream=None):
         sh = self.shape
+        self._qdraft = qdraft
+        if self.scoring == "tc":
+            ob.oasis_score_blocks_tc(self.kmin, self.kmax, sh.Nb_max, qdraft, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D,
+                                     seq_len, sh.W, self.scores, self.radius, self.status, stream)
+            return
         ob.oasis_score_blocks(self.kmin, self.kmax, sh.Nb_max, qdraft, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D,
                               seq_len, sh.W, self.scores, self.status, stream)
 
-    def select(self, seq_len, stream=None):
+    def select(self, seq_len, stream=None, qdraft=None):
+        """qdraft: the drafts of the preceding score() call (the default); the
+        tensor-core path recomputes the scores its decisions need from them."""
         sh = self.shape
+        if self.scoring == "tc":
+            qd = qdraft if qdraft is not None else self._qdraft
+            if qd is None:
+                raise RuntimeError("select() before score(): the tc selection needs the draft queries")
+            ob.oasis_select_topk_capped_tc(self.scores, self.radius, self.kmin, self.kmax, qd, sh.G, sh.Nd, sh.D,
+                                           sh.Nb_max, seq_len, sh.B, sh.Hkv, sh.K, sh.W, sh.cap, self.table,
+                                           self.table_next, self.plan, self.plan_count, self.status, stream)
+            return
         ob.oasis_select_topk_capped(self.scores, sh.Nb_max, seq_len, sh.B, sh.Hkv, sh.K, sh.W, sh.cap,
                                     self.table, self.table_next, self.plan, self.plan_count, self.status, stream)
 
@@ -152,7 +178,7 @@ class DecodeLayer:
 
         timed("attn", fg, lambda: self.attend(q, seq_len, stream=fg))
         timed("score", bg, lambda: self.score(qdraft, seq_len, stream=bg))
-        timed("select", bg, lambda: self.select(seq_len, stream=bg))
+        timed("select", bg, lambda: self.select(seq_len, stream=bg, qdraft=qdraft))
         e_fg, e_bg = torch.cuda.Event(), torch.cuda.Event()
         e_fg.record(fg)
         e_bg.record(bg)
@@ -329,7 +355,7 @@ class DecodeStepGraph:
                 if new_keys is not None:
                     lay.build_summary(self.new_keys[i], self.seq_len, blk_begin=new_block, blk_count=1, stream=bg)
                 lay.score(self.qdraft[i], self.seq_len, stream=bg)
-                lay.select(self.seq_len, stream=bg)
+                lay.select(self.seq_len, stream=bg, qdraft=self.qdraft[i])
                 e_sel = torch.cuda.Event()
                 e_sel.record(bg)
                 lay.attend(self.q[i], self.seq_len, stream=fg)

@@ -76,8 +76,8 @@ def test_decode_step_graph_parity(host_io):
         assert g.h2d_bytes >= R * (q.numel() + qd.numel() + new_keys.numel()) * 2
 
 
-@pytest.mark.parametrize("host_io", [False, True])
-def test_decode_steps_advance_over_drift_steps(host_io):
+@pytest.mark.parametrize("host_io,scoring", [(False, "exact"), (True, "exact"), (False, "tc"), (True, "tc")])
+def test_decode_steps_advance_over_drift_steps(host_io, scoring):
     """The benchmarked form: one graph per drift step, tables advancing, the
     graphs replayed in drift order; after several decode steps every layer's
     table, plan, pool and attention output equal the oracle chained over the
@@ -99,7 +99,7 @@ def test_decode_steps_advance_over_drift_steps(host_io):
     strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
     lays = []
     for _ in range(R):
-        lay = okv.DecodeLayer(shape)
+        lay = okv.DecodeLayer(shape, scoring=scoring)
         lay.build_summary(tiles, sl, 0, w.Nb, strides=strides)
         lays.append(lay)
     new_keys = tiles[:, w.Nb - 1:w.Nb, 0].contiguous()
