@@ -72,7 +72,7 @@ extern "C" {
 /* cudaStream_t without including the CUDA headers (it is this same type). */
 typedef struct CUstream_st *oasis_stream_t;
 
-#define OASIS_ABI_VERSION 1
+#define OASIS_ABI_VERSION 2
 
 /* Return codes. */
 #define OASIS_OK 0
@@ -114,6 +114,11 @@ int oasis_abi_version(void);
  * seq_len:  int32 [B] valid tokens per sequence (device).
  * kmin/kmax: summary arrays (layout above), written for every block of the
  *           range that holds a valid token; other entries are not touched.
+ * wsum:     optional (NULL: not written) float32 [S][Nb_max]: for the same
+ *           blocks, an upper bound (within a relative 2^-14) of the sum over
+ *           the dims of the summary values on the wrong side of zero, |kmax_d|
+ *           where kmax_d < 0 plus kmin_d where kmin_d > 0.  Not part of the
+ *           method: oasis_score_blocks_tc reads it to bound its rounding.
  * Per dim, over the block's valid tokens: kmin = IEEE minimum, kmax = IEEE
  * maximum, with -0 below +0.  Exact (no rounding).  NaN keys: undefined.
  * EINVAL: a NULL pointer, D not 64 or 128, B or Hkv < 1, Nb_max < 1,
@@ -122,7 +127,8 @@ int oasis_abi_version(void);
  */
 int oasis_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
                         int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
-                        uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, oasis_stream_t stream);
+                        uint16_t *kmin, uint16_t *kmax, float *wsum, int Nb_max, int32_t *status,
+                        oasis_stream_t stream);
 
 /*
  * Look-ahead block scores: the draft queries of each KV head scan its
@@ -156,19 +162,24 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
  * scores[s][b] = s~, radius[s][b] = r (both float32 [S][Nb_max]), written
  * for the same candidate blocks as oasis_score_blocks, such that the score s
  * that oasis_score_blocks computes for the block satisfies |s~ - s| <= r.
- *   r = 2^-12 (|s~| + 2 C) + 2^-110,  C = sum_d Q_d c_d,
+ *   r = 2^-12 (|s~| + 2 C) + 2^-110,  C >= sum_d Q_d c_d,
  * Q_d = max over the head's query vectors of |q_d|, c_d = |kmax_d| where
- * kmax_d < 0, kmin_d where kmin_d > 0, else 0.  The sum of the absolute terms
- * of any query is at most |s~| + 2C (up to rounding), and both the fixed-order
- * fp32 sum and the tensor cores' fp32 accumulation of 2D terms stay within
- * 2^-16 of it, so r carries a margin of 16.  A NaN score gets radius +inf.
+ * kmax_d < 0 plus kmin_d where kmin_d > 0, else 0.  The sum of the absolute
+ * terms of any query is at most |s~| + 2C (up to rounding), and both the
+ * fixed-order fp32 sum and the tensor cores' fp32 accumulation of 2D terms
+ * stay within 2^-16 of it, so r carries a margin of 16.  A NaN score gets
+ * radius +inf.
+ * wsum:     optional; the sums oasis_build_summary keeps for these summaries.
+ *           Given: C = (max_d Q_d) * wsum[s][b].  NULL: C = sum_d Q_d c_d,
+ *           read from the summaries (slower when many blocks have a dim on the
+ *           wrong side of zero).
  * oasis_select_topk_capped_tc turns these into the exact selection.
  * Host-side checks, alignment and EINVAL cases: as oasis_score_blocks, plus
  * radius (4-byte aligned, not NULL).  One CTA per SM with about 200 KB of
  * shared memory; every internal wait is bounded (OASIS_STATUS_TIMEOUT).
  */
-int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
-                          int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
+int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                          const uint16_t *qdraft, int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
                           float *scores, float *radius, int32_t *status, oasis_stream_t stream);
 
 /*

@@ -48,9 +48,9 @@ _F = ctypes.c_float
 _SIGS = {
     "oasis_strerror": (ctypes.c_char_p, [_I]),
     "oasis_abi_version": (_I, []),
-    "oasis_build_summary": (_I, [_P, _I64, _I64, _I64, _I, _I, _I, _P, _I, _I, _P, _P, _I, _P, _P]),
+    "oasis_build_summary": (_I, [_P, _I64, _I64, _I64, _I, _I, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P]),
     "oasis_score_blocks": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
-    "oasis_score_blocks_tc": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
+    "oasis_score_blocks_tc": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "oasis_select_topk_capped": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "oasis_select_topk_capped_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                         _P]),
@@ -114,10 +114,10 @@ def abi_version() -> int:
 
 
 def oasis_build_summary(k, seg_stride, blk_stride, tok_stride, B, Hkv, D, seq_len, blk_begin, blk_count,
-                        kmin, kmax, Nb_max, status=None, stream=None):
+                        kmin, kmax, Nb_max, status=None, stream=None, wsum=None):
     return _check("oasis_build_summary", load().oasis_build_summary(
         _ptr(k), seg_stride, blk_stride, tok_stride, B, Hkv, D, _ptr(seq_len), blk_begin, blk_count,
-        _ptr(kmin), _ptr(kmax), Nb_max, _ptr(status), _stream(stream)))
+        _ptr(kmin), _ptr(kmax), _ptr(wsum), Nb_max, _ptr(status), _stream(stream)))
 
 
 def oasis_score_blocks(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, status=None,
@@ -128,9 +128,9 @@ def oasis_score_blocks(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W,
 
 
 def oasis_score_blocks_tc(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores, radius, status=None,
-                          stream=None):
+                          stream=None, wsum=None):
     return _check("oasis_score_blocks_tc", load().oasis_score_blocks_tc(
-        _ptr(kmin), _ptr(kmax), Nb_max, _ptr(qdraft), B, Hkv, G, Nd, D, _ptr(seq_len), W, _ptr(scores),
+        _ptr(kmin), _ptr(kmax), _ptr(wsum), Nb_max, _ptr(qdraft), B, Hkv, G, Nd, D, _ptr(seq_len), W, _ptr(scores),
         _ptr(radius), _ptr(status), _stream(stream)))
 
 

@@ -52,6 +52,22 @@ cudaError_t raise_smem_limit(const void *fn, size_t smem) {
   return cudaSuccess;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to
+// the driver library); nullptr when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
 cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm) {
   struct Entry {
     const void *fn;
@@ -111,17 +127,17 @@ int oasis_abi_version(void) { return OASIS_ABI_VERSION; }
 
 int oasis_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride, int B,
                         int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count, uint16_t *kmin,
-                        uint16_t *kmax, int Nb_max, int32_t *status, oasis_stream_t stream) {
+                        uint16_t *kmax, float *wsum, int Nb_max, int32_t *status, oasis_stream_t stream) {
   if (!k || !seq_len || !kmin || !kmax) return OASIS_EINVAL;
   if (!d_ok(D) || !segs_ok(B, Hkv) || Nb_max < 1) return OASIS_EINVAL;
   if (blk_begin < 0 || blk_count < 0 || static_cast<int64_t>(blk_begin) + blk_count > Nb_max) return OASIS_EINVAL;
   if (seg_stride < 0 || blk_stride < 0 || tok_stride < 0) return OASIS_EINVAL;
   if ((seg_stride | blk_stride | tok_stride) & 7) return OASIS_EINVAL;
   if (!aligned16(k) || !aligned16(kmin) || !aligned16(kmax) || !aligned4(seq_len)) return OASIS_EINVAL;
-  if (status && !aligned4(status)) return OASIS_EINVAL;
+  if ((status && !aligned4(status)) || (wsum && !aligned4(wsum))) return OASIS_EINVAL;
   if (blk_count == 0) return OASIS_OK;
   return finish(oasis::launch_build_summary(k, seg_stride, blk_stride, tok_stride, B, Hkv, D, seq_len, blk_begin,
-                                            blk_count, kmin, kmax, Nb_max, status, stream));
+                                            blk_count, kmin, kmax, wsum, Nb_max, status, stream));
 }
 
 int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
@@ -137,17 +153,17 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
                                            status, stream));
 }
 
-int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
-                          int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W, float *scores,
-                          float *radius, int32_t *status, oasis_stream_t stream) {
+int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                          const uint16_t *qdraft, int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
+                          float *scores, float *radius, int32_t *status, oasis_stream_t stream) {
   if (!kmin || !kmax || !qdraft || !seq_len || !scores || !radius) return OASIS_EINVAL;
   if (!d_ok(D) || !segs_ok(B, Hkv) || Nb_max < 1 || W < 0) return OASIS_EINVAL;
   if (G < 1 || G > 16 || Nd < 1 || G * Nd > 64) return OASIS_EINVAL;
   if (!aligned16(kmin) || !aligned16(kmax) || !aligned16(qdraft) || !aligned4(seq_len) || !aligned4(scores) ||
       !aligned4(radius))
     return OASIS_EINVAL;
-  if (status && !aligned4(status)) return OASIS_EINVAL;
-  return finish(oasis::launch_score_blocks_tc(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores,
+  if ((status && !aligned4(status)) || (wsum && !aligned4(wsum))) return OASIS_EINVAL;
+  return finish(oasis::launch_score_blocks_tc(kmin, kmax, wsum, Nb_max, qdraft, B, Hkv, G, Nd, D, seq_len, W, scores,
                                               radius, status, stream));
 }
 

@@ -682,20 +682,6 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 template <int KS, int NT>
 cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                      const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,

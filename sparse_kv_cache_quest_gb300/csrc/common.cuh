@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "oasis.h"
@@ -125,16 +127,19 @@ struct LaunchCfg {
 // Launchers implemented by the kernel translation units (host side).
 namespace oasis {
 cudaError_t raise_smem_limit(const void *fn, size_t smem);
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 cudaError_t launch_geometry(const void *fn, int threads, size_t smem, int *sms, int *per_sm);
 cudaError_t launch_build_summary(const uint16_t *k, int64_t seg_stride, int64_t blk_stride, int64_t tok_stride,
                                  int B, int Hkv, int D, const int32_t *seq_len, int blk_begin, int blk_count,
-                                 uint16_t *kmin, uint16_t *kmax, int Nb_max, int32_t *status, cudaStream_t st);
+                                 uint16_t *kmin, uint16_t *kmax, float *wsum, int Nb_max, int32_t *status,
+                                 cudaStream_t st);
 cudaError_t launch_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
                                 int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
                                 float *scores, int32_t *status, cudaStream_t st);
-cudaError_t launch_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
-                                   int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
-                                   float *scores, float *radius, int32_t *status, cudaStream_t st);
+cudaError_t launch_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                                   const uint16_t *qdraft, int B, int Hkv, int G, int Nd, int D,
+                                   const int32_t *seq_len, int W, float *scores, float *radius, int32_t *status,
+                                   cudaStream_t st);
 cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                                       oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st);

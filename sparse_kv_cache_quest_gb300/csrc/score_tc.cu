@@ -28,23 +28,28 @@
 //
 // Work split: the tiles (128 consecutive candidate blocks of one segment) of
 // all segments form one range, split evenly over a persistent grid of one CTA
-// per SM.  Roles in a CTA (warp-specialised, mbarrier hand-offs, every wait
-// bounded):
-//   warp 0, one lane  - bulk copies of a tile's 2*D/8 chunks (16 bytes per
-//                       block per 8 dims, contiguous over the tile's blocks in
-//                       the chunk-major summary layout) into a ring of stages;
-//   warp 1, one lane  - the 2D/16 MMAs of a tile into one of two TMEM
+// per SM.  A tile is moved in two halves (its kmax chunks, then its kmin
+// chunks; 32 KiB each at d_h 128) through a ring of half-tile stages.  Roles in
+// a CTA (warp-specialised, mbarrier hand-offs, every wait bounded):
+//   warp 0, one lane  - one 3-D TMA tensor copy per half-tile (a box of 16
+//                       chunks x 128 blocks x 8 dims of the chunk-major
+//                       summaries; 16-byte bulk copies per chunk when the block
+//                       count is not a multiple of 8);
+//   warp 1, one lane  - D/16 MMAs per half-tile into one of four TMEM
 //                       accumulators (the warp also owns the TMEM allocation);
-//   warps 2-5         - per segment, the split query operand {q+, q-} in the
-//                       no-swizzle K-major layout and Q_d (two buffers, built
-//                       one segment ahead); per tile, C_b from the stage (each
-//                       thread one block row), then the accumulator row from
-//                       TMEM (tcgen05.ld), the max over the columns, the radius,
-//                       and the stores.
+//   warps 2-5 (scan)  - per segment, the split query operand {q+, q-} in the
+//                       no-swizzle K-major layout and Q_d (two buffers, built one
+//                       segment ahead); per half-tile, C_b's share from the stage
+//                       (each thread one block row), then the stage is released;
+//                       C_b goes to the TMEM warps through a small ring;
+//   warps 6-9 (TMEM)  - the accumulator row (tcgen05.ld), the max over the
+//                       columns, the radius, the stores.
+// The scan warps move with the copies and the TMEM warps with the MMAs, so
+// neither holds up the other's ring.
 // Shared-memory operands use the no-swizzle K-major layout of 8-row x 16-byte
 // core matrices: the chunk-major summaries already are that layout (chunk c of
-// 128 blocks = 16 core matrices at 128-byte steps), so a tile lands by plain
-// bulk copies: LBO (next 8 K-elements) = 2048 bytes, SBO (next 8 rows) = 128.
+// 128 blocks = 16 core matrices at 128-byte steps), so a half-tile lands as is:
+// LBO (next 8 K-elements) = 2048 bytes, SBO (next 8 rows) = 128.
 #include <algorithm>
 #include <cfloat>
 
@@ -54,11 +59,14 @@ namespace oasis {
 namespace {
 
 constexpr int kRows = 128;                    // blocks per tile (MMA M)
-constexpr int kEpiWarps = 4;
-constexpr int kThreadsTC = 32 * (2 + kEpiWarps);
+constexpr int kGroupWarps = 4;                // scan warps, and TMEM warps
+constexpr int kThreadsTC = 32 * (2 + 2 * kGroupWarps);
+constexpr int kNAcc = 4;                      // TMEM accumulators
+constexpr int kNC = 4;                        // C_b hand-off ring (scan -> TMEM warps)
 constexpr uint32_t kChunkBytes = kRows * 16;  // one 8-dim chunk of a tile
 constexpr uint32_t kWaitTriesTC = 1u << 22;   // bounded mbarrier polls (far beyond any real copy or MMA)
 constexpr size_t kSmemCap = 227 * 1024;
+constexpr int kMaxStages = 8;
 
 // ---- tcgen05 / TMEM primitives (inline PTX, sm_100a family) -----------------
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -107,7 +115,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory"); }
+__device__ __forceinline__ void scan_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kGroupWarps) : "memory"); }
+// one 3-D tensor copy (x, y, z) into this CTA's shared memory, completing on bar
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
 
 // Bounded wait that also gives up once another role has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -125,6 +141,12 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 __device__ __forceinline__ uint32_t neg_halves(uint32_t x) {
   uint32_t r;
   asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(r) : "r"(x));
+  return r;
+}
+// max with NaN propagation (either input NaN -> NaN)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
 
@@ -153,26 +175,35 @@ struct TileIter {
     }
     return t1;
   }
+  // does segment s have a work tile in [t0, t1)?
+  __device__ bool active(int s) const {
+    const int64_t first = std::max<int64_t>(t0, static_cast<int64_t>(s) * tps);
+    return static_cast<int>(first - static_cast<int64_t>(s) * tps) * kRows < nc_of(s);
+  }
 };
 
 template <int N, int CH>
 __global__ void __launch_bounds__(kThreadsTC, 1)
-    k_score_tc(const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax, int Nb_max,
-               const uint16_t *__restrict__ qdraft, int S, int Hkv, int G, int Nd,
-               const int32_t *__restrict__ seq_len, int W, float *__restrict__ scores, float *__restrict__ radius,
-               int32_t *status, int tps, int stages) {
+    k_score_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmn, bool use_tma,
+               const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax,
+               const float *__restrict__ wsum, int Nb_max, const uint16_t *__restrict__ qdraft, int S, int Hkv,
+               int G, int Nd, const int32_t *__restrict__ seq_len, int W, float *__restrict__ scores,
+               float *__restrict__ radius, int32_t *status, int tps, int stages) {
   constexpr int D = CH * 8;
-  constexpr int KS = 2 * D / 16;                       // MMAs per tile (K = 16 each)
-  constexpr uint32_t kATile = 2u * CH * kChunkBytes;   // kmax chunks then kmin chunks
+  constexpr int KH = D / 16;                           // MMAs per half-tile (K = 16 each)
+  constexpr uint32_t kHalf = CH * kChunkBytes;         // one half-tile: the kmax chunks or the kmin chunks
   constexpr uint32_t kBBytes = static_cast<uint32_t>(N) * 2 * D * 2;
-  constexpr uint32_t kTmemCols = 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : 128);
+  constexpr uint32_t kTmemCols = kNAcc * N <= 64 ? 64 : (kNAcc * N <= 128 ? 128 : 256);
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *sA = smem;                                               // [stages][kATile]
-  uint8_t *sB = sA + static_cast<size_t>(stages) * kATile;          // [2][kBBytes]
+  uint8_t *sA = smem;                                               // [stages][kHalf]
+  uint8_t *sB = sA + static_cast<size_t>(stages) * kHalf;           // [2][kBBytes]
   float *sQ = reinterpret_cast<float *>(sB + 2 * kBBytes);          // [2][D]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sQ + 2 * D);        // full[st], empty[st], accF[2], accE[2], bq[2]
-  uint64_t *full = bars, *empty = bars + stages, *accF = bars + 2 * stages, *accE = accF + 2, *bqF = accE + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bqF + 2);
+  float *sC = sQ + 2 * D;                                           // [kNC][kRows]
+  float *sQmax = sC + kNC * kRows;                                  // [2]: max_d Q_d per query buffer
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sQmax + 2);
+  uint64_t *full = bars, *empty = full + stages, *accF = empty + stages, *accE = accF + kNAcc;
+  uint64_t *bqF = accE + kNAcc, *bqE = bqF + 2, *cF = bqE + 2, *cE = cF + kNC, *drain = cE + kNC;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -190,13 +221,22 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (tid == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + kEpiWarps);  // the MMAs' commit + each epilogue warp's scan
+      // the MMAs' commit, plus each scan warp when it reads the stage (no wsum)
+      mbar_init(&empty[i], wsum != nullptr ? 1 : 1 + kGroupWarps);
+    }
+    for (int i = 0; i < kNAcc; ++i) {
+      mbar_init(&accF[i], 1);
+      mbar_init(&accE[i], kGroupWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&accF[i], 1);
-      mbar_init(&accE[i], kEpiWarps);
-      mbar_init(&bqF[i], 32 * kEpiWarps);
+      mbar_init(&bqF[i], 32 * kGroupWarps);
+      mbar_init(&bqE[i], 1);
     }
+    for (int i = 0; i < kNC; ++i) {
+      mbar_init(&cF[i], 32 * kGroupWarps);
+      mbar_init(&cE[i], kGroupWarps);
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -221,29 +261,40 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
 
   if (warp == 0) {
-    // ---------------- producer: bulk copies of the tiles into the stage ring
+    // ---------------- producer: one copy per half-tile into the stage ring
     if (lane == 0) {
-      int64_t issued = 0;
+      int64_t issued = 0;  // half-tiles
       int nc = 0;
-      for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
+      bool ok = true;
+      for (int64_t t = it.next(it.t0, &nc); t < it.t1 && ok; t = it.next(t + 1, &nc)) {
         const int s = static_cast<int>(t / tps);
         const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
         const int rows = min(kRows, nc - base);
-        const int st = static_cast<int>(issued % stages);
-        if (issued >= stages &&
-            !wait_or_abort(&empty[st], static_cast<uint32_t>((issued / stages) - 1) & 1u, abort_flag))
-          break;
-        const uint32_t bytes = static_cast<uint32_t>(rows) * 16u;
-        mbar_arrive_expect_tx(&full[st], 2u * CH * bytes);
-        uint8_t *dst = sA + static_cast<size_t>(st) * kATile;
-        const uint4 *gx = reinterpret_cast<const uint4 *>(kmax) + static_cast<int64_t>(s) * CH * Nb_max + base;
-        const uint4 *gn = reinterpret_cast<const uint4 *>(kmin) + static_cast<int64_t>(s) * CH * Nb_max + base;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int st = static_cast<int>(issued % stages);
+          if (issued >= stages &&
+              !wait_or_abort(&empty[st], static_cast<uint32_t>((issued / stages) - 1) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t *dst = sA + static_cast<size_t>(st) * kHalf;
+          if (use_tma) {
+            // box {8 blocks x 8 dims, 16 groups of 8 blocks, CH chunks}: rows past
+            // the summary capacity arrive zero-filled, so the byte count is fixed
+            mbar_arrive_expect_tx(&full[st], kHalf);
+            tma_load_3d(dst, h == 0 ? &tmx : &tmn, 0, base / 8, s * CH, &full[st]);
+          } else {
+            const uint32_t bytes = static_cast<uint32_t>(rows) * 16u;
+            mbar_arrive_expect_tx(&full[st], CH * bytes);
+            const uint4 *g = reinterpret_cast<const uint4 *>(h == 0 ? kmax : kmin) +
+                             static_cast<int64_t>(s) * CH * Nb_max + base;
 #pragma unroll 4
-        for (int c = 0; c < CH; ++c) {
-          bulk_g2s(dst + c * kChunkBytes, gx + static_cast<int64_t>(c) * Nb_max, bytes, &full[st]);
-          bulk_g2s(dst + (CH + c) * kChunkBytes, gn + static_cast<int64_t>(c) * Nb_max, bytes, &full[st]);
+            for (int c = 0; c < CH; ++c)
+              bulk_g2s(dst + c * kChunkBytes, g + static_cast<int64_t>(c) * Nb_max, bytes, &full[st]);
+          }
+          ++issued;
         }
-        ++issued;
       }
       // never leave with copies in flight: wait for the last stages issued
       for (int64_t k = std::max<int64_t>(0, issued - stages); k < issued; ++k)
@@ -253,164 +304,240 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<N>();
-      int64_t i = 0;
+      int64_t i = 0, u = 0;  // tiles, half-tiles
       int seg_prev = -1, nseg = 0, buf = 0;
       int nc = 0;
       bool ok = true;
       for (int64_t t = it.next(it.t0, &nc); t < it.t1 && ok; t = it.next(t + 1, &nc)) {
         const int s = static_cast<int>(t / tps);
         if (s != seg_prev) {  // the query operand of this segment
+          if (seg_prev >= 0) tc_commit(&bqE[buf]);  // the previous segment's operand is free once its MMAs are done
           buf = nseg & 1;
           ok = wait_or_abort(&bqF[buf], static_cast<uint32_t>(nseg >> 1) & 1u, abort_flag);
           ++nseg;
           seg_prev = s;
           if (!ok) break;
         }
-        const int st = static_cast<int>(i % stages);
-        const int acc = static_cast<int>(i & 1);
-        ok = wait_or_abort(&full[st], static_cast<uint32_t>(i / stages) & 1u, abort_flag);
-        if (ok && i >= 2) ok = wait_or_abort(&accE[acc], static_cast<uint32_t>((i >> 1) - 1) & 1u, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t a0 = smem_addr(sA + static_cast<size_t>(st) * kATile);
+        const int acc = static_cast<int>(i % kNAcc);
+        if (i >= kNAcc &&
+            !wait_or_abort(&accE[acc], static_cast<uint32_t>((i / kNAcc) - 1) & 1u, abort_flag))
+          break;
         const uint32_t b0 = smem_addr(sB + static_cast<size_t>(buf) * kBBytes);
+#pragma unroll 1
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int st = static_cast<int>(u % stages);
+          ok = wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(sA + static_cast<size_t>(st) * kHalf);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint64_t da = smem_desc(a0 + kk * 2 * kChunkBytes, kChunkBytes, 128);
-          const uint64_t db = smem_desc(b0 + kk * 2 * (N * 16), N * 16, 128);
-          tc_mma(tmem + static_cast<uint32_t>(acc * N), da, db, idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < KH; ++kk) {
+            const int kg = h * KH + kk;  // K-step within the tile: kmax part, then kmin part
+            const uint64_t da = smem_desc(a0 + kk * 2 * kChunkBytes, kChunkBytes, 128);
+            const uint64_t db = smem_desc(b0 + kg * 2 * (N * 16), N * 16, 128);
+            tc_mma(tmem + static_cast<uint32_t>(acc * N), da, db, idesc, kg > 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[st]);  // the half-stage is free once these MMAs have read it
+          ++u;
         }
-        tc_commit(&empty[st]);
+        if (!ok) break;
         tc_commit(&accF[acc]);
         ++i;
       }
-      // every MMA issued has completed before the accumulators are released:
-      // the last commit arrives on accF of the last tile
-      if (i > 0) mbar_wait_bounded(&accF[(i - 1) & 1], static_cast<uint32_t>((i - 1) >> 1) & 1u, kWaitTriesTC);
+      // every MMA issued has completed before the tensor memory is released
+      // (also after giving up half-way through a tile)
+      if (u > 0) {
+        tc_commit(drain);
+        mbar_wait_bounded(drain, 0u, kWaitTriesTC);
+      }
     }
-  } else {
-    // ---------------- epilogue warps: query operands, radii, TMEM -> scores
+  } else if (warp < 2 + kGroupWarps) {
+    // ---------------- scan warps: query operands, C_b, stage release
     const int et = tid - 64;                   // 0 .. 127
-    const int quad = warp & 3;                 // the TMEM lane quadrant this warp may access
-    const int row = quad * 32 + lane;          // the tile row (block) this thread owns
+    const int row = (warp & 3) * 32 + lane;    // the tile row (block) this thread owns
     const int Nq = G * Nd, Hq = Hkv * G;
     const int s_first = static_cast<int>(it.t0 / tps);
     const int s_last = it.t1 > it.t0 ? static_cast<int>((it.t1 - 1) / tps) : s_first - 1;
     int next_build = s_first, built = 0;
-    // does segment s have a work tile in [t0, t1)?
-    auto active = [&](int s) {
-      const int64_t first = std::max<int64_t>(it.t0, static_cast<int64_t>(s) * tps);
-      return static_cast<int>(first - static_cast<int64_t>(s) * tps) * kRows < it.nc_of(s);
-    };
     // build {q+, q-} and Q of the next active segment into buffer built & 1
+    constexpr int kItems = (N * CH + 32 * kGroupWarps - 1) / (32 * kGroupWarps);  // 16-byte query pieces per thread
     auto build_next = [&]() {
-      while (next_build <= s_last && !active(next_build)) ++next_build;
+      while (next_build <= s_last && !it.active(next_build)) ++next_build;
       if (next_build > s_last) return;
       const int s = next_build, bq = built & 1;
       const int bseq = s / Hkv, h = s % Hkv;
       uint8_t *B = sB + static_cast<size_t>(bq) * kBBytes;
       float *Q = sQ + bq * D;
-      epi_barrier();  // every epilogue thread is done with this buffer's previous segment
-      for (int d = et; d < D; d += 32 * kEpiWarps) Q[d] = 0.0f;
-      epi_barrier();
-      for (int item = et; item < N * CH; item += 32 * kEpiWarps) {
-        const int n = item / CH, c = item % CH;
-        const int j = min(n, Nq - 1), jd = j / G, g = j % G;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-            qdraft + ((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + c * 8));
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t pos[4], neg[4];
+      uint4 raw[kItems];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t m = neg_halves(w4[e]);
-          neg[e] = w4[e] & m;
-          pos[e] = w4[e] & ~m;
-          // Q_d = max over the queries of |q_d| (non-negative floats order as integers)
-          atomicMax(reinterpret_cast<unsigned int *>(Q) + c * 8 + 2 * e, (w4[e] & 0x7FFFu) << 16);
-          atomicMax(reinterpret_cast<unsigned int *>(Q) + c * 8 + 2 * e + 1, w4[e] & 0x7FFF0000u);
+      for (int k = 0; k < kItems; ++k) {  // every load in flight before the first use
+        const int item = et + k * 32 * kGroupWarps;
+        if (item < N * CH) {
+          const int n = item / CH, c = item % CH;
+          const int j = min(n, Nq - 1), jd = j / G, g = j % G;
+          raw[k] = __ldg(reinterpret_cast<const uint4 *>(
+              qdraft + ((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + c * 8));
         }
-        *reinterpret_cast<uint4 *>(B + c * (N * 16) + n * 16) = make_uint4(pos[0], pos[1], pos[2], pos[3]);
-        *reinterpret_cast<uint4 *>(B + (CH + c) * (N * 16) + n * 16) = make_uint4(neg[0], neg[1], neg[2], neg[3]);
+      }
+      // the MMAs of the segment two back (same buffer) have completed (after an
+      // abort the wait returns at once; the outputs are then void anyway)
+      if (built >= 2) wait_or_abort(&bqE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
+      scan_barrier();  // every scan thread is done with this buffer's previous segment
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const int item = et + k * 32 * kGroupWarps;
+        if (item < N * CH) {
+          const int n = item / CH, c = item % CH;
+          const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+          uint32_t pos[4], neg[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t m = neg_halves(w4[e]);
+            neg[e] = w4[e] & m;
+            pos[e] = w4[e] & ~m;
+          }
+          *reinterpret_cast<uint4 *>(B + c * (N * 16) + n * 16) = make_uint4(pos[0], pos[1], pos[2], pos[3]);
+          *reinterpret_cast<uint4 *>(B + (CH + c) * (N * 16) + n * 16) = make_uint4(neg[0], neg[1], neg[2], neg[3]);
+        }
       }
       fence_proxy_async_smem();  // the tensor cores read B through the async proxy
       mbar_arrive(&bqF[bq]);
-      epi_barrier();             // Q is complete for every epilogue thread
+      scan_barrier();
+      // Q_d = max over the query columns of |q_d|: a thread per pair of dims (non-
+      // negative bf16 values order as integers; q+ and q- hold one of them each)
+      for (int p = et; p < D / 2; p += 32 * kGroupWarps) {
+        const int c = p / 4, e = p % 4;
+        const uint32_t *colp = reinterpret_cast<const uint32_t *>(B + c * (N * 16)) + e;
+        const uint32_t *coln = reinterpret_cast<const uint32_t *>(B + (CH + c) * (N * 16)) + e;
+        uint32_t m = 0;
+#pragma unroll 8
+        for (int n = 0; n < N; ++n) m = __vmaxu2(m, (colp[n * 4] | coln[n * 4]) & 0x7FFF7FFFu);
+        Q[2 * p] = bf16_lo(m);
+        Q[2 * p + 1] = bf16_hi(m);
+      }
+      scan_barrier();  // Q is complete for every scan thread
+      if (et == 0) {
+        float qm = 0.0f;
+        for (int d = 0; d < D; ++d) qm = fmaxf(qm, Q[d]);
+        sQmax[bq] = qm;
+      }
+      scan_barrier();
       ++next_build;
       ++built;
     };
     build_next();
     build_next();
-    int64_t i = 0;
+    // The group never leaves this loop early: after an abort every wait returns
+    // at once and the work is skipped, so all four warps meet at the same named
+    // barriers (inside build_next) whatever happened.
+    int64_t i = 0, u = 0;  // tiles, half-tiles
     int seg_prev = -1, used = 0, bq = 0;
     int nc = 0;
-    const float gamma = 0x1p-12f, floor_r = 0x1p-110f;
     for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
       const int s = static_cast<int>(t / tps);
       if (s != seg_prev) {
-        if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is free
+        if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is rebuilt for the next-but-one
         bq = used & 1;
         ++used;
         seg_prev = s;
       }
       const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
       const int rows = min(kRows, nc - base);
-      const int st = static_cast<int>(i % stages);
-      const int acc = static_cast<int>(i & 1);
-      if (!wait_or_abort(&full[st], static_cast<uint32_t>(i / stages) & 1u, abort_flag)) break;
-      // C_b: the summary values on the wrong side of zero, weighted by Q_d
+      // C_b: the summary values on the wrong side of zero, weighted by Q_d (kmax
+      // half: |kmax| where kmax < 0; kmin half: kmin where kmin > 0).  With wsum
+      // (their per-block sum, kept by the summary build) C_b <= max_d Q_d * wsum
+      // and the stages are not read here.
       float C = 0.0f;
-      if (row < rows) {
-        const uint8_t *A = sA + static_cast<size_t>(st) * kATile + row * 16;
-        const float *Q = sQ + bq * D;
-#pragma unroll 4
-        for (int c = 0; c < CH; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
-          const uint4 y = *reinterpret_cast<const uint4 *>(A + (CH + c) * kChunkBytes);
-          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-          uint32_t any = 0, nw[4], pw[4];
+      if (wsum != nullptr) {
+        if (row < rows) C = sQmax[bq] * __ldg(wsum + static_cast<int64_t>(s) * Nb_max + base + row);
+      } else {
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int st = static_cast<int>(u % stages);
+          const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u,
+                                                                 abort_flag));
+          if (got && row < rows) {
+            const uint8_t *A = sA + static_cast<size_t>(st) * kHalf + row * 16;
+            // fast test: any sign bit set among the kmax half (h = 0) / any clear among
+            // the kmin half (h = 1)?  (-0 and +0 pass it too; their magnitude is 0)
+            uint32_t acc_or = 0u, acc_and = 0xFFFFFFFFu;
+#pragma unroll 8
+            for (int c = 0; c < CH; ++c) {
+              const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
+              acc_or |= x.x | x.y | x.z | x.w;
+              acc_and &= x.x & x.y & x.z & x.w;
+            }
+            const bool wrong = h == 0 ? (acc_or & 0x80008000u) != 0u : (acc_and & 0x80008000u) != 0x80008000u;
+            if (wrong) {  // the exact weighted sum
+              const float *Q = sQ + bq * D;
+              for (int c = 0; c < CH; ++c) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            nw[e] = xs[e] & neg_halves(xs[e]) & 0x7FFF7FFFu;  // |kmax| where kmax < 0
-            pw[e] = ys[e] & ~neg_halves(ys[e]);               // kmin where kmin > 0
-            any |= nw[e] | pw[e];
-          }
-          if (any) {
-            const float *q = Q + c * 8;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              C = fmaf(q[2 * e], bf16_lo(nw[e]) + bf16_lo(pw[e]), C);
-              C = fmaf(q[2 * e + 1], bf16_hi(nw[e]) + bf16_hi(pw[e]), C);
+                for (int e = 0; e < 4; ++e) {
+                  const uint32_t m = neg_halves(xs[e]);
+                  const uint32_t cw = h == 0 ? (xs[e] & m & 0x7FFF7FFFu) : (xs[e] & ~m);
+                  C = fmaf(Q[c * 8 + 2 * e], bf16_lo(cw), C);
+                  C = fmaf(Q[c * 8 + 2 * e + 1], bf16_hi(cw), C);
+                }
+              }
             }
           }
+          __syncwarp();
+          if (got && lane == 0) mbar_arrive(&empty[st]);
+          ++u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (!wait_or_abort(&accF[acc], static_cast<uint32_t>(i >> 1) & 1u, abort_flag)) break;
+      const int cb = static_cast<int>(i % kNC);
+      const bool room = i < kNC || __all_sync(0xFFFFFFFFu, wait_or_abort(&cE[cb], static_cast<uint32_t>((i / kNC) - 1) &
+                                                                                     1u, abort_flag));
+      if (room) {
+        sC[cb * kRows + row] = C;
+        mbar_arrive(&cF[cb]);
+      }
+      ++i;
+    }
+  } else {
+    // ---------------- TMEM warps: accumulator row -> max -> radius -> stores
+    const int quad = warp & 3;                 // the TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    int64_t i = 0;
+    int nc = 0;
+    const float gamma = 0x1p-12f, floor_r = 0x1p-110f;
+    for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
+      const int s = static_cast<int>(t / tps);
+      const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
+      const int rows = min(kRows, nc - base);
+      const int acc = static_cast<int>(i % kNAcc);
+      if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&accF[acc], static_cast<uint32_t>(i / kNAcc) & 1u, abort_flag)))
+        break;  // the whole warp leaves together
       tc_fence_after();
       float best = -FLT_MAX;
-      bool nan = false;
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * N);
 #pragma unroll
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t r[16];
         tmem_ld16(taddr + c0, r);
+        float m8[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float v = __uint_as_float(r[k]);
-          nan |= v != v;
-          best = fmaxf(best, v);
-        }
+        for (int k = 0; k < 8; ++k) m8[k] = max_nan(__uint_as_float(r[k]), __uint_as_float(r[k + 8]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m8[k] = max_nan(m8[k], m8[k + 4]);
+        best = max_nan(best, max_nan(max_nan(m8[0], m8[1]), max_nan(m8[2], m8[3])));
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accE[acc]);
+      const int cb = static_cast<int>(i % kNC);
+      if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&cF[cb], static_cast<uint32_t>(i / kNC) & 1u, abort_flag))) break;
+      const float C = sC[cb * kRows + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cE[cb]);
       if (row < rows) {
-        const float sc = nan ? __uint_as_float(0x7FC00000u) : best;
-        const float rad = fmaf(gamma, fabsf(best) + 2.0f * C, floor_r);
+        const bool nan = best != best;
         const int64_t o = static_cast<int64_t>(s) * Nb_max + base + row;
-        scores[o] = sc;
-        radius[o] = nan ? __uint_as_float(0x7F800000u) : rad;
+        scores[o] = best;
+        radius[o] = nan ? __uint_as_float(0x7F800000u) : fmaf(gamma, fabsf(best) + 2.0f * C, floor_r);
       }
       ++i;
     }
@@ -425,51 +552,80 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   }
 }
 
+// The summaries of one kind (kmin or kmax) as a 3-D tensor: x = 64 bf16 (8
+// consecutive blocks of one 8-dim chunk, 128 bytes), y = Nb_max / 8 groups of 8
+// blocks, z = S * CH chunks; one box = a half-tile.
+int make_summary_map(CUtensorMap *m, const uint16_t *base, int S, int CH, int Nb_max) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return -1;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(Nb_max / 8), static_cast<cuuint64_t>(S) * CH};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(Nb_max) * 16};
+  const cuuint32_t box[3] = {64, kRows / 8, static_cast<cuuint32_t>(CH)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? 0
+             : -1;
+}
+
 template <int N, int CH>
-cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
-                      int Hkv, int G, int Nd, const int32_t *seq_len, int W, float *scores, float *radius,
-                      int32_t *status, cudaStream_t st) {
+cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                      const uint16_t *qdraft, int B, int Hkv, int G, int Nd, const int32_t *seq_len, int W,
+                      float *scores, float *radius, int32_t *status, cudaStream_t st) {
   constexpr int D = CH * 8;
-  constexpr size_t kATile = 2u * CH * kChunkBytes;
+  constexpr size_t kHalf = static_cast<size_t>(CH) * kChunkBytes;
   constexpr size_t kBBytes = static_cast<size_t>(N) * 2 * D * 2;
   const int S = B * Hkv;
   const int ncand = Nb_max - W;
   if (ncand <= 0) return cudaSuccess;  // no candidate can exist
   const int tps = (ncand + kRows - 1) / kRows;
-  const size_t fixed = 2 * kBBytes + 2 * D * sizeof(float) + 16 * sizeof(uint64_t) + 64;
-  const int stages = static_cast<int>(std::min<size_t>(4, (kSmemCap - fixed) / kATile));
+  // A tile's rows read by the tensor copies may run past Nb_max (zero-filled);
+  // the tensor view needs whole groups of 8 blocks, else 16-byte bulk copies
+  CUtensorMap tmx{}, tmn{};
+  const bool use_tma = Nb_max % 8 == 0 && make_summary_map(&tmx, kmax, S, CH, Nb_max) == 0 &&
+                       make_summary_map(&tmn, kmin, S, CH, Nb_max) == 0;
+  const size_t fixed = 2 * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
+                       (2 * kMaxStages + 2 * kNAcc + 4 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
+  const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kHalf));
   if (stages < 2) return cudaErrorInvalidValue;
-  const size_t smem = fixed + stages * kATile + 1024;  // + alignment slack of the dynamic base
+  const size_t smem = fixed + stages * kHalf;
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score_tc<N, CH>), kThreadsTC, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t T = static_cast<int64_t>(S) * tps;
   const int grid = static_cast<int>(std::min<int64_t>(sms, T));
   LaunchCfg lc(dim3(grid), dim3(kThreadsTC), smem, st);
-  return cudaLaunchKernelEx(&lc.cfg, k_score_tc<N, CH>, kmin, kmax, Nb_max, qdraft, S, Hkv, G, Nd, seq_len, W,
-                            scores, radius, status, tps, stages);
+  return cudaLaunchKernelEx(&lc.cfg, k_score_tc<N, CH>, tmx, tmn, use_tma, kmin, kmax, wsum, Nb_max, qdraft, S,
+                            Hkv, G, Nd, seq_len, W, scores, radius, status, tps, stages);
 }
 
 template <int CH>
-cudaError_t launch_tc_n(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft, int B,
-                        int Hkv, int G, int Nd, const int32_t *seq_len, int W, float *scores, float *radius,
-                        int32_t *status, cudaStream_t st) {
+cudaError_t launch_tc_n(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                        const uint16_t *qdraft, int B, int Hkv, int G, int Nd, const int32_t *seq_len, int W,
+                        float *scores, float *radius, int32_t *status, cudaStream_t st) {
   const int Nq = G * Nd;
-  if (Nq <= 16) return launch_tc<16, CH>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
-  if (Nq <= 32) return launch_tc<32, CH>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
-  if (Nq <= 48) return launch_tc<48, CH>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
-  if (Nq <= 64) return launch_tc<64, CH>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
+#define OASIS_TC_CASE(NN)                                                                                       \
+  if (Nq <= NN)                                                                                                  \
+    return launch_tc<NN, CH>(kmin, kmax, wsum, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, \
+                             st);
+  OASIS_TC_CASE(16)
+  OASIS_TC_CASE(32)
+  OASIS_TC_CASE(48)
+  OASIS_TC_CASE(64)
+#undef OASIS_TC_CASE
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, const uint16_t *qdraft,
-                                   int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
-                                   float *scores, float *radius, int32_t *status, cudaStream_t st) {
+cudaError_t launch_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
+                                   const uint16_t *qdraft, int B, int Hkv, int G, int Nd, int D,
+                                   const int32_t *seq_len, int W, float *scores, float *radius, int32_t *status,
+                                   cudaStream_t st) {
   if (D == 128)
-    return launch_tc_n<16>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
-  return launch_tc_n<8>(kmin, kmax, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
+    return launch_tc_n<16>(kmin, kmax, wsum, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
+  return launch_tc_n<8>(kmin, kmax, wsum, Nb_max, qdraft, B, Hkv, G, Nd, seq_len, W, scores, radius, status, st);
 }
 
 }  // namespace oasis

@@ -89,6 +89,20 @@ struct SelScalars {
 
 static_assert(sizeof(SelScalars) + 3 * 256 * sizeof(uint32_t) <= kStaticSmemBound, "static shared memory bound");
 
+// Sum of v over the CTA (all threads call it, all get the sum).
+__device__ int block_sum(int v, int *warp_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();  // warp_tot may still be read by a previous use
+  if (lane == 0) warp_tot[warp] = v;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < kWarps; ++w) t += warp_tot[w];
+  __syncthreads();
+  return t;
+}
+
 // T as a bitmap: the first min(K, nc) candidates by (key desc, block asc).
 // 4-pass 8-bit MSB radix select of the K-th largest key (warp-aggregated
 // shared-memory histograms, triple-buffered so each pass takes one barrier),
@@ -194,6 +208,26 @@ __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, 
 // exactly, so every set equals the one the exact scores give.
 constexpr int kBatch = 32;  // blocks recomputed per pass
 
+// Byte offsets of the certified kernel's extra shared memory, from the start
+// of the dynamic allocation; one definition serves the kernel's pointers and
+// the launcher's allocation size.
+struct CertLayout {
+  size_t stage, qsm, res, bmX, xl, rankE, end;
+};
+__host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max, int K, int CH, int Nq) {
+  const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
+  const size_t Nq4 = (static_cast<size_t>(Nq) + 3) & ~static_cast<size_t>(3);
+  CertLayout L;
+  L.stage = (base_bytes + 15) & ~static_cast<size_t>(15);
+  L.qsm = L.stage + 16 * static_cast<size_t>(kBatch) * (2 * CH + 1);      // uint4 [kBatch][2*CH + 1]
+  L.res = L.qsm + 4 * static_cast<size_t>(CH) * 8 * Nq4;                 // float [D][Nq4]
+  L.bmX = L.res + 4 * static_cast<size_t>(kBatch) * Nq4;                 // float [kBatch][Nq4]
+  L.xl = L.bmX + 4 * words;                                              // uint32 [words]
+  L.rankE = L.xl + 4 * static_cast<size_t>(Nb_max);                      // int32 [Nb_max]
+  L.end = L.rankE + 4 * static_cast<size_t>(K);                          // int32 [K]
+  return L;
+}
+
 struct CertArgs {
   float *scores;  // in: estimates; out: the recomputed blocks' fixed-order scores
   const float *radius;
@@ -220,12 +254,16 @@ __device__ float block_reduce(float v, bool is_max, float *red) {
 // arithmetic: per query, sum over d ascending from +0 of q_d * (q_d >= 0 ?
 // kmax_d : kmin_d), one rounding per term; max over the queries, NaN kept).
 // Writes them to srow and their keys to keys, marks them in bmX.
+// A thread takes one block and four queries (the widened summary values serve
+// all four); qsm holds the queries as [d][Nq4], Nq4 = Nq rounded up to 4, the
+// padding repeating the last query.
 template <int CH>
 __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
                                  int Nq, const float *qsm, uint4 *stage, float *res, float *srow, uint32_t *keys,
                                  uint32_t *bmX, SelScalars &sc) {
   constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
   const int tid = threadIdx.x;
+  const int Nq4 = (Nq + 3) & ~3, ng = Nq4 / 4;
   for (int e0 = 0; e0 < n; e0 += kBatch) {
     const int nb = min(kBatch, n - e0);
     for (int i = tid; i < nb * 2 * CH; i += kThreads) {
@@ -234,29 +272,35 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
       stage[e * ES + k] = __ldg((k < CH ? gmin : gmax) + static_cast<int64_t>(c) * Nb_max + b);
     }
     __syncthreads();
-    for (int i = tid; i < nb * Nq; i += kThreads) {
-      const int e = i / Nq, j = i % Nq;
+    for (int i = tid; i < nb * ng; i += kThreads) {
+      const int e = i / ng, g = i % ng;
       const uint4 *st = stage + e * ES;
-      float acc = 0.0f;
-#pragma unroll 2
+      const float *qg = qsm + 4 * g;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
       for (int c = 0; c < CH; ++c) {
         const uint4 mn = st[c], mx = st[CH + c];
         const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w}, wx[4] = {mx.x, mx.y, mx.z, mx.w};
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          const float q = qsm[(c * 8 + t) * Nq + j];
-          const uint32_t w = q >= 0.0f ? wx[t >> 1] : wn[t >> 1];
-          acc = fmaf(q, (t & 1) ? bf16_hi(w) : bf16_lo(w), acc);  // exact product, one rounding
+          const float kn = (t & 1) ? bf16_hi(wn[t >> 1]) : bf16_lo(wn[t >> 1]);
+          const float kx = (t & 1) ? bf16_hi(wx[t >> 1]) : bf16_lo(wx[t >> 1]);
+          const float4 q = *reinterpret_cast<const float4 *>(qg + (c * 8 + t) * Nq4);
+          acc[0] = fmaf(q.x, q.x >= 0.0f ? kx : kn, acc[0]);  // exact product, one rounding
+          acc[1] = fmaf(q.y, q.y >= 0.0f ? kx : kn, acc[1]);
+          acc[2] = fmaf(q.z, q.z >= 0.0f ? kx : kn, acc[2]);
+          acc[3] = fmaf(q.w, q.w >= 0.0f ? kx : kn, acc[3]);
         }
       }
-      res[e * Nq + j] = acc;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) res[e * Nq4 + 4 * g + k] = acc[k];
     }
     __syncthreads();
     for (int e = tid; e < nb; e += kThreads) {
       float best = -INFINITY;
       bool nan = false;
       for (int j = 0; j < Nq; ++j) {
-        const float v = res[e * Nq + j];
+        const float v = res[e * Nq4 + j];
         nan |= v != v;
         best = fmaxf(best, v);
       }
@@ -315,14 +359,14 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   // certified selection only (sized by cert_smem_bytes)
   constexpr int D = CH * 8;
   const int Nq = CERTIFY ? ca.G * ca.Nd : 0;
-  unsigned char *craw = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(fSorted + cap) + 15) & ~static_cast<uintptr_t>(15));
-  uint4 *stage = reinterpret_cast<uint4 *>(craw);                  // [kBatch][2*CH + 1]
-  float *qsm = reinterpret_cast<float *>(stage + kBatch * (2 * CH + 1));  // [D][Nq]
-  float *res = qsm + D * Nq;                                       // [kBatch][Nq]
-  uint32_t *bmX = reinterpret_cast<uint32_t *>(res + kBatch * Nq); // [words] recomputed blocks
-  int32_t *xl = reinterpret_cast<int32_t *>(bmX + words);          // [Nb_max] blocks to recompute
-  int32_t *rankE = xl + Nb_max;                                    // [K]
+  const int Nq4 = (Nq + 3) & ~3;
+  const CertLayout cl = cert_layout(reinterpret_cast<unsigned char *>(fSorted + cap) - smraw, Nb_max, K, CH, Nq);
+  uint4 *stage = reinterpret_cast<uint4 *>(smraw + cl.stage);      // staged summaries of recomputed blocks
+  float *qsm = reinterpret_cast<float *>(smraw + cl.qsm);          // [D][Nq4] queries
+  float *res = reinterpret_cast<float *>(smraw + cl.res);          // [kBatch][Nq4] per-query sums
+  uint32_t *bmX = reinterpret_cast<uint32_t *>(smraw + cl.bmX);    // [words] recomputed blocks
+  int32_t *xl = reinterpret_cast<int32_t *>(smraw + cl.xl);        // [Nb_max] blocks to recompute
+  int32_t *rankE = reinterpret_cast<int32_t *>(smraw + cl.rankE);  // [K]
   float *srow_w = CERTIFY ? ca.scores + static_cast<int64_t>(s) * Nb_max : nullptr;
   const float *rrow = CERTIFY ? ca.radius + static_cast<int64_t>(s) * Nb_max : nullptr;
   const uint4 *gmin = CERTIFY ? reinterpret_cast<const uint4 *>(ca.kmin) + static_cast<int64_t>(s) * CH * Nb_max
@@ -346,15 +390,16 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
   if constexpr (CERTIFY) {
     for (int i = tid; i < words; i += kThreads) bmX[i] = 0u;
-    // the segment's query vectors, widened: qsm[d][j], j = draft * G + head in group
-    const int Hq = Hkv * ca.G, bseq = s / Hkv, h = s % Hkv;
-    for (int i = tid; i < Nq * CH; i += kThreads) {
-      const int j = i / CH, c = i % CH, jd = j / ca.G, g = j % ca.G;
+    // the segment's query vectors, widened: qsm[d][j], j = draft * G + head in group,
+    // padded to a multiple of 4 by repeating the last one
+    const int Hq = Hkv * ca.G, bseq = s / Hkv, h = s % Hkv, Nq4 = (Nq + 3) & ~3;
+    for (int i = tid; i < Nq4 * CH; i += kThreads) {
+      const int j = i / CH, c = i % CH, jq = min(j, Nq - 1), jd = jq / ca.G, g = jq % ca.G;
       const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
           ca.qdraft + ((static_cast<int64_t>(bseq) * ca.Nd + jd) * Hq + h * ca.G + g) * D + c * 8));
       const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int t = 0; t < 8; ++t) qsm[(c * 8 + t) * Nq + j] = (t & 1) ? bf16_hi(w4[t >> 1]) : bf16_lo(w4[t >> 1]);
+      for (int t = 0; t < 8; ++t) qsm[(c * 8 + t) * Nq4 + j] = (t & 1) ? bf16_hi(w4[t >> 1]) : bf16_lo(w4[t >> 1]);
     }
   }
   bool nan = false;
@@ -414,13 +459,39 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       }
       __syncthreads();
       recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, bmX, sc);
-      for (int i = tid; i < words; i += kThreads) bmT[i] = 0u;
-      for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
+      // T = the settled members of the estimated T, and as many of the recomputed
+      // ones as the estimated T held, best first by the exact keys
+      int need = 0;
+      for (int i = tid; i < nX; i += kThreads) need += bit(bmT, xl[i]);
+      need = block_sum(need, sc.warp_tot);
+      for (int i = warp; i < nX; i += kWarps) {
+        const int b = xl[i];
+        const uint64_t ci = composite(keys[b], b);
+        int r = 0;
+        for (int j0 = 0; j0 < nX; j0 += 32) {
+          const int j = j0 + lane;
+          r += __popc(__ballot_sync(0xFFFFFFFFu, j < nX && composite(keys[xl[j]], xl[j]) > ci));
+        }
+        if (lane == 0) {
+          const uint32_t m = 1u << (b & 31);
+          if (r < need)
+            atomicOr(&bmT[b >> 5], m);
+          else
+            atomicAnd(&bmT[b >> 5], ~m);
+        }
+      }
+      __syncthreads();
+    }
+  } else {
+    topk_bitmap(keys, nc, K, bmT, hist, sc);
+    __syncthreads();
+  }
+  if constexpr (CERTIFY) {
+    if (nc <= K) {
+      topk_bitmap(keys, nc, K, bmT, hist, sc);  // every candidate
       __syncthreads();
     }
   }
-  topk_bitmap(keys, nc, K, bmT, hist, sc);
-  __syncthreads();
 
   // 4. lists: N = T \ R (candidates to admit), E = R \ T (residents that may go)
   for (int b = tid; b < nc; b += kThreads) {
@@ -598,13 +669,6 @@ size_t select_smem_bytes(int Nb_max, int K, int W, int cap) {
          sizeof(int32_t) * (static_cast<size_t>(K + W) + 2 * K + 3 * static_cast<size_t>(cap));
 }
 
-// the certified kernel's extra shared memory (after the above, 16-byte aligned)
-size_t cert_smem_bytes(int Nb_max, int K, int D, int Nq) {
-  const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
-  const size_t CH = static_cast<size_t>(D) / 8;
-  return 16 + sizeof(uint4) * kBatch * (2 * CH + 1) + sizeof(float) * (static_cast<size_t>(D) * Nq + kBatch * Nq) +
-         sizeof(uint32_t) * words + sizeof(int32_t) * (static_cast<size_t>(Nb_max) + K);
-}
 
 cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
@@ -622,7 +686,7 @@ cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int
 }
 
 size_t select_tc_smem_bytes(int Nb_max, int K, int W, int cap, int D, int Nq) {
-  return select_smem_bytes(Nb_max, K, W, cap) + cert_smem_bytes(Nb_max, K, D, Nq);
+  return cert_layout(select_smem_bytes(Nb_max, K, W, cap), Nb_max, K, D / 8, Nq).end;
 }
 
 cudaError_t launch_select_topk_capped_tc(float *scores, const float *radius, const uint16_t *kmin,

@@ -84,6 +84,9 @@ class DecodeLayer:
             raise ValueError(f"scoring must be 'exact' or 'tc', not {scoring!r}")
         self.scoring = scoring
         self.radius = torch.zeros_like(self.scores) if scoring == "tc" else None
+        # per-block sums of the summary values on the wrong side of zero, kept by the
+        # summary build for the tensor-core scoring's error bound
+        self.wsum = torch.zeros_like(self.scores) if scoring == "tc" else None
         self._qdraft = None                   # the drafts the last score() call read (the tc selection rereads them)
 
     # -- individual steps ---------------------------------------------------
@@ -97,14 +100,14 @@ class DecodeLayer:
             seg, blk, tok = strides
         n = keys.shape[1] if blk_count is None else blk_count
         ob.oasis_build_summary(keys, seg, blk, tok, sh.B, sh.Hkv, sh.D, seq_len, blk_begin, n,
-                               self.kmin, self.kmax, sh.Nb_max, self.status, stream)
+                               self.kmin, self.kmax, sh.Nb_max, self.status, stream, wsum=self.wsum)
 
     def score(self, qdraft, seq_len, stream=None):
         sh = self.shape
         self._qdraft = qdraft
         if self.scoring == "tc":
             ob.oasis_score_blocks_tc(self.kmin, self.kmax, sh.Nb_max, qdraft, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D,
-                                     seq_len, sh.W, self.scores, self.radius, self.status, stream)
+                                     seq_len, sh.W, self.scores, self.radius, self.status, stream, wsum=self.wsum)
             return
         ob.oasis_score_blocks(self.kmin, self.kmax, sh.Nb_max, qdraft, sh.B, sh.Hkv, sh.G, sh.Nd, sh.D,
                               seq_len, sh.W, self.scores, self.status, stream)

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(ob.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
-    assert okv.abi_version() == 1
+    assert okv.abi_version() == 2
 
 
 def test_strerror(lib):
@@ -44,7 +44,10 @@ def _einval(fn, *args):
     assert e.value.code == ob.EINVAL
 
 
-P = 1 << 20   # a 16-byte aligned fake address; every call below fails validation first
+# A 16-byte aligned fake address.  Every call below is rejected by a check that
+# looks only at the arguments themselves (null, alignment, ranges, sizes from the
+# same device-independent formula), before anything reads device state.
+P = 1 << 20
 
 
 def test_build_summary_validation(lib):
@@ -55,6 +58,8 @@ def test_build_summary_validation(lib):
     _einval(f, P + 2, 0, 0, 0, 1, 1, 128, P, 0, 1, P, P, 4, None, 0)     # misaligned keys
     _einval(f, None, 0, 0, 0, 1, 1, 128, P, 0, 1, P, P, 4, None, 0)      # NULL
     _einval(f, P, 0, 0, 0, 0, 1, 128, P, 0, 1, P, P, 4, None, 0)         # B
+    with pytest.raises(ob.OasisError):                                    # misaligned wrong-side sums
+        f(P, 0, 0, 0, 1, 1, 128, P, 0, 1, P, P, 4, None, 0, wsum=P + 2)
 
 
 def test_score_validation(lib):
@@ -64,6 +69,26 @@ def test_score_validation(lib):
     _einval(f, P, P, 16, P, 1, 1, 4, 1, 128, P, -1, P, None, 0)          # W < 0
     _einval(f, P, P, 0, P, 1, 1, 4, 1, 128, P, 0, P, None, 0)            # Nb_max
     _einval(f, P, P, 16, P + 8, 1, 1, 4, 1, 128, P, 0, P, None, 0)       # qdraft not 16-byte aligned
+
+
+def test_score_tc_validation(lib):
+    f = okv.oasis_score_blocks_tc
+    _einval(f, P, P, 16, P, 1, 1, 17, 1, 128, P, 0, P, P, None, 0)       # G > 16
+    _einval(f, P, P, 16, P, 1, 1, 16, 5, 128, P, 0, P, P, None, 0)       # G*Nd > 64
+    _einval(f, P, P, 16, P, 1, 1, 4, 1, 96, P, 0, P, P, None, 0)         # D
+    _einval(f, P, P, 16, P, 1, 1, 4, 1, 128, P, 0, P, None, None, 0)     # radius required
+    _einval(f, P, P, 16, P, 1, 1, 4, 1, 128, P, 0, P, P + 2, None, 0)    # radius misaligned
+
+
+def test_select_tc_validation(lib):
+    f = okv.oasis_select_topk_capped_tc
+    #   scores radius kmin kmax qd  G  Nd  D  Nb_max sl  B  Hkv K  W  cap tin tout plan cnt status
+    _einval(f, P, P, P, P, P, 4, 1, 128, 20000, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)   # Nb_max > 16384
+    _einval(f, P, P, P, P, P, 4, 1, 96, 64, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)       # D
+    _einval(f, P, P, P, P, P, 17, 1, 128, 64, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)     # G
+    _einval(f, P, None, P, P, P, 4, 1, 128, 64, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)   # radius
+    _einval(f, P, P, P + 8, P, P, 4, 1, 128, 64, P, 1, 1, 8, 0, 2, P, P, P, P, P, 0)  # kmin alignment
+    _einval(f, P, P, P, P, P, 4, 1, 128, 64, P, 1, 1, 8, 0, 9, P, P, P, P, P, 0)      # cap > K
 
 
 def test_select_validation(lib):

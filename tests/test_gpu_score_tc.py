@@ -4,9 +4,11 @@
 
 * Every estimate lies within its radius of the fixed-order score of
   oasis_score_blocks (itself bit-exact against the oracle), on the workloads'
-  shapes, ragged lengths, d_h 64, and adversarial summaries (one-signed
-  channels, heavy cancellation), with a margin: the observed error stays below
-  1/16 of the radius.
+  shapes, ragged lengths, d_h 64, and adversarial keys (one-signed channels,
+  heavy cancellation), with a margin: the observed error stays below 1/16 of
+  the radius - both with the per-block wrong-side sums the summary build keeps
+  (wsum) and without them (read from the summaries in the kernel).
+* wsum is an upper bound within 2^-13 of the exact sum.
 * The certified selection gives exactly the tables, plans and counts of the
   exact path, and the scores it recomputes are bit-identical to the
   fixed-order ones; the same holds with the radii inflated (more
@@ -35,23 +37,24 @@ CASES = {
 }
 
 
-def _summaries(w, seq_len=None):
-    tiles = device_tiles(w, 0)
+def _summaries(w, seq_len=None, tiles=None):
+    tiles = device_tiles(w, 0) if tiles is None else tiles
     sl = (wl.seq_lens(w) if seq_len is None else seq_len).cuda()
     kmin = torch.zeros((w.S, w.D // 8, w.Nb, 8), dtype=torch.bfloat16, device="cuda")
     kmax = torch.zeros_like(kmin)
+    wsum = torch.full((w.S, w.Nb), -7.0, dtype=torch.float32, device="cuda")
     okv.oasis_build_summary(tiles, tiles.stride(0), tiles.stride(1), tiles.stride(3), w.B, w.Hkv, w.D, sl, 0, w.Nb,
-                            kmin, kmax, w.Nb)
-    return tiles, sl, kmin, kmax
+                            kmin, kmax, w.Nb, wsum=wsum)
+    return tiles, sl, kmin, kmax, wsum
 
 
-def _score_both(w, kmin, kmax, qd, sl):
+def _score_both(w, kmin, kmax, qd, sl, wsum=None):
     exact = torch.full((w.S, w.Nb), -7.0, dtype=torch.float32, device="cuda")
     est = torch.full_like(exact, -7.0)
     rad = torch.full_like(exact, -7.0)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     okv.oasis_score_blocks(kmin, kmax, w.Nb, qd, w.B, w.Hkv, w.G, w.Nd, w.D, sl, w.W, exact, status)
-    okv.oasis_score_blocks_tc(kmin, kmax, w.Nb, qd, w.B, w.Hkv, w.G, w.Nd, w.D, sl, w.W, est, rad, status)
+    okv.oasis_score_blocks_tc(kmin, kmax, w.Nb, qd, w.B, w.Hkv, w.G, w.Nd, w.D, sl, w.W, est, rad, status, wsum=wsum)
     torch.cuda.synchronize()
     assert status.item() == 0, okv.strerror(status.item())
     return exact, est, rad
@@ -76,14 +79,36 @@ def _check_radius(w, sl, exact, est, rad, margin=16.0):
     return worst
 
 
+def _wrong_side_sums(w, kmin, kmax):
+    """float64 [S][Nb]: sum over dims of |kmax| where kmax < 0 plus kmin where kmin > 0."""
+    f = lambda t: torch.from_numpy(bits(t.permute(0, 2, 1, 3).reshape(w.S, w.Nb, w.D)).astype(np.uint32) << 16)  # noqa
+    mn = f(kmin).numpy().view(np.float32).astype(np.float64)
+    mx = f(kmax).numpy().view(np.float32).astype(np.float64)
+    return (np.where(mx < 0, -mx, 0.0) + np.where(mn > 0, mn, 0.0)).sum(axis=-1)
+
+
 @pytest.mark.parametrize("name", list(CASES))
-def test_estimates_within_radius(name):
+@pytest.mark.parametrize("with_wsum", [True, False])
+def test_estimates_within_radius(name, with_wsum):
     okv.load()
     w = CASES[name]
-    _, sl, kmin, kmax = _summaries(w)
+    _, sl, kmin, kmax, wsum = _summaries(w)
     qd = wl.drafts(w, 0).cuda()
-    exact, est, rad = _score_both(w, kmin, kmax, qd, sl)
+    exact, est, rad = _score_both(w, kmin, kmax, qd, sl, wsum if with_wsum else None)
     _check_radius(w, sl, exact, est, rad)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3-235b-8seq", "d64-64q"])
+def test_wrong_side_sums_bound(name):
+    okv.load()
+    w = CASES[name]
+    _, sl, kmin, kmax, wsum = _summaries(w)
+    ref = _wrong_side_sums(w, kmin, kmax)
+    got = wsum.cpu().numpy().astype(np.float64)
+    nc = w.nc
+    assert np.all(got[:, :nc] >= ref[:, :nc])
+    assert np.all(got[:, :nc] <= ref[:, :nc] * (1 + 2.0 ** -13))
+    assert np.all(got[:, nc:] == -7.0)
 
 
 def test_estimates_within_radius_ragged_and_empty():
@@ -93,42 +118,40 @@ def test_estimates_within_radius_ragged_and_empty():
     sl[1] = 0                                    # an empty sequence
     sl[2] = 16 * 128                             # exactly one full tile
     sl[3] = 16 * 129 + 3                         # a tile and a ragged tail
-    _, sld, kmin, kmax = _summaries(w, sl)
+    _, sld, kmin, kmax, wsum = _summaries(w, sl)
     qd = wl.drafts(w, 0).cuda()
-    exact, est, rad = _score_both(w, kmin, kmax, qd, sld)
-    _check_radius(w, sld, exact, est, rad)
+    for ws in (wsum, None):
+        exact, est, rad = _score_both(w, kmin, kmax, qd, sld, ws)
+        _check_radius(w, sld, exact, est, rad)
 
 
 def _adversarial(w, seed):
-    """Summaries with one-signed channels (kmin > 0 or kmax < 0) and queries
-    that make the terms cancel: the radius must cover sum |terms|, far above
-    the score itself."""
+    """Keys with one-signed channels (every token of a block above or below zero
+    there) and a few blocks of large keys, and queries that make the terms
+    cancel: the radius must cover sum |terms|, far above the score itself."""
     g = torch.Generator().manual_seed(seed)
     S, D, Nb = w.S, w.D, w.Nb
-    a = torch.randn((S, Nb, D), generator=g)
-    b = torch.randn((S, Nb, D), generator=g)
-    kmin, kmax = torch.minimum(a, b), torch.maximum(a, b)
+    k = torch.randn((S, Nb, 16, D), generator=g)
     pos = torch.randperm(D, generator=g)[:D // 4]     # channels whose keys are all positive
     neg = torch.randperm(D, generator=g)[:D // 8]     # ... all negative
-    kmin[..., pos] = kmin[..., pos].abs() + 4.0
-    kmax[..., pos] = kmin[..., pos] + kmax[..., pos].abs()
-    kmax[..., neg] = -(kmax[..., neg].abs() + 4.0)
-    kmin[..., neg] = kmax[..., neg] - kmin[..., neg].abs()
+    k[..., pos] = k[..., pos].abs() + 4.0
+    k[..., neg] = -(k[..., neg].abs() + 4.0)
     big = torch.randperm(Nb, generator=g)[:Nb // 16]   # a few blocks with large values
-    kmin[:, big] *= 64.0
-    kmax[:, big] *= 64.0
+    k[:, big] *= 64.0
+    tiles = torch.zeros((S, Nb, 2, 16, D), dtype=torch.bfloat16)
+    tiles[:, :, 0] = k.to(torch.bfloat16)
     q = torch.randn((w.B, w.Nd, w.Hq, D), generator=g) * 3.0
-    to_cm = lambda t: t.to(torch.bfloat16).view(S, Nb, D // 8, 8).permute(0, 2, 1, 3).contiguous().cuda()  # noqa
-    return to_cm(kmin), to_cm(kmax), q.to(torch.bfloat16).cuda()
+    _, sl, kmin, kmax, wsum = _summaries(w, tiles=tiles.cuda())
+    return sl, kmin, kmax, wsum, q.to(torch.bfloat16).cuda()
 
 
 @pytest.mark.parametrize("seed", [1, 2, 3])
-def test_radius_covers_one_signed_channels_and_cancellation(seed):
+@pytest.mark.parametrize("with_wsum", [True, False])
+def test_radius_covers_one_signed_channels_and_cancellation(seed, with_wsum):
     okv.load()
     w = wl.WORKLOADS[5].with_(B=2, L=16 * 700)
-    kmin, kmax, qd = _adversarial(w, seed)
-    sl = wl.seq_lens(w).cuda()
-    exact, est, rad = _score_both(w, kmin, kmax, qd, sl)
+    sl, kmin, kmax, wsum, qd = _adversarial(w, seed)
+    exact, est, rad = _score_both(w, kmin, kmax, qd, sl, wsum if with_wsum else None)
     _check_radius(w, sl, exact, est, rad)
     # the wrong-side term is active: radii well above 2^-12 |estimate|
     r, a = rad.cpu().numpy(), est.cpu().numpy()
@@ -151,8 +174,8 @@ def _select(w, sl, scores, table0, tc=None):
     return tout.cpu(), plan.cpu(), cnt.cpu(), int(status.item())
 
 
-def _compare_selection(w, sl, kmin, kmax, qd, table0, inflate=(1.0, 1e3, float("inf"))):
-    exact, est, rad = _score_both(w, kmin, kmax, qd, sl)
+def _compare_selection(w, sl, kmin, kmax, qd, table0, inflate=(1.0, 1e3, float("inf")), wsum=None):
+    exact, est, rad = _score_both(w, kmin, kmax, qd, sl, wsum)
     ref = _select(w, sl, exact, table0)
     assert ref[3] == 0
     e_np = exact.cpu().numpy()
@@ -175,12 +198,12 @@ def _compare_selection(w, sl, kmin, kmax, qd, table0, inflate=(1.0, 1e3, float("
 def test_certified_selection_equals_exact(name):
     okv.load()
     w = CASES[name]
-    tiles, sl, kmin, kmax = _summaries(w)
+    tiles, sl, kmin, kmax, wsum = _summaries(w)
     segs = sample_segments(w)
     tiles_cpu = {s: bits(tiles[s]) for s in segs}
     table0 = prior_tables(w, 0, set(segs), lambda s: tiles_cpu[s], wl.seq_lens(w)).cuda()
     qd = wl.drafts(w, 0).cuda()
-    recomputed, ref = _compare_selection(w, sl, kmin, kmax, qd, table0)
+    recomputed, ref = _compare_selection(w, sl, kmin, kmax, qd, table0, wsum=wsum)
     if w.nc > w.K:
         # with the true radii only a small part of the candidates is recomputed
         assert recomputed[0] < 0.25 * w.S * w.nc, recomputed
@@ -198,7 +221,7 @@ def test_certified_selection_on_ties_and_ragged_lengths():
     w = wl.WORKLOADS[5].with_(B=4)
     sl = wl.ragged_seq_lens(w, 16 * 100)
     sl[1] = 16 * 60                                       # fewer candidates than K
-    tiles, sld, kmin, kmax = _summaries(w, sl)
+    tiles, sld, kmin, kmax, wsum = _summaries(w, sl)
     # exact ties: many blocks share one summary (the rank among them is by block id)
     for s in range(w.S):
         kmin[s, :, 100:160] = kmin[s, :, 99:100]
@@ -209,14 +232,13 @@ def test_certified_selection_on_ties_and_ragged_lengths():
         row = [b if b < nc else -1 for b in table0[s].tolist()]
         table0[s] = torch.tensor(row, dtype=torch.int32)
     qd = wl.drafts(w, 0).cuda()
-    _compare_selection(w, sld, kmin, kmax, qd, table0.cuda())
+    _compare_selection(w, sld, kmin, kmax, qd, table0.cuda())   # no wsum: the copied summaries have none
 
 
 @pytest.mark.parametrize("seed", [4, 5])
 def test_certified_selection_on_adversarial_summaries(seed):
     okv.load()
     w = wl.WORKLOADS[5].with_(B=2, L=16 * 700, K=64)
-    kmin, kmax, qd = _adversarial(w, seed)
-    sl = wl.seq_lens(w).cuda()
+    sl, kmin, kmax, wsum, qd = _adversarial(w, seed)
     table0 = torch.stack([wl.prior_random(w, 0, s) for s in range(w.S)]).cuda()
-    _compare_selection(w, sl, kmin, kmax, qd, table0)
+    _compare_selection(w, sl, kmin, kmax, qd, table0, wsum=wsum)
