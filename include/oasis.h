@@ -308,15 +308,16 @@ int oasis_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool, const i
 /*
  * oasis_sparse_decode_attn_ws without caller memory: the partial results and
  * arrival counters live in a scratch array of 8 MiB that the library holds in
- * device memory per device (a static device variable, looked up once per
- * device; nothing is allocated or freed by the call).  The paper has no
+ * device memory per device (a static device variable whose address is looked
+ * up once per CUDA context - a context made after a device reset gets its own
+ * lookup; nothing is allocated or freed by the call).  The paper has no
  * counterpart: this is a convenience of this library for callers that cannot
  * provide a workspace.  Same arguments and results as oasis_sparse_decode_attn.
  * The counters are cleared at the start of every call (a 4-byte-per-segment
  * memset on `stream`).  Calls that may overlap in time on one device (other
  * streams, other host threads) race on the shared scratch: serialise them on
  * one stream or use oasis_sparse_decode_attn_ws with separate workspaces.
- * The first call on a device should not be inside a stream capture (it looks
+ * The first call in a context should not be inside a stream capture (it looks
  * up the scratch's device address).
  * EINVAL: as oasis_sparse_decode_attn, or a shape whose workspace
  * (oasis_attn_workspace_bytes) exceeds the 8 MiB scratch.

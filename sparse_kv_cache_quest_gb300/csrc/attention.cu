@@ -42,6 +42,8 @@
 #include <algorithm>
 #include <cfloat>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 
@@ -743,7 +745,7 @@ int64_t bal_grid(int64_t N) {
 template <int KS, int NT>
 cudaError_t launch_bal_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                          const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
-                         int32_t *status, float *part, int32_t *counter, cudaStream_t st) {
+                         int32_t *status, float *part, int32_t *counter, int64_t P, cudaStream_t st) {
   constexpr int D = 16 * KS;
   using PL = Plan<D, 8 * NT>;
   const int S = B * Hkv;
@@ -763,8 +765,7 @@ cudaError_t launch_bal_t(const uint16_t *q, const uint16_t *pool, const int32_t 
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn_bal<KS, NT>), kThreads, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t N = static_cast<int64_t>(S) * slots;
-  const int64_t P = bal_grid(N);
-  if (P > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  if (P < 1 || P > N || P > 0x7FFFFFFF) return cudaErrorInvalidValue;
   LaunchCfg lc(dim3(static_cast<unsigned>(P)), dim3(kThreads), smem, st);
   const float scale_log2 = scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&lc.cfg, k_attn_bal<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out,
@@ -784,35 +785,53 @@ cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, c
   return launch_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
 }
 
-size_t attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg) {
+// Workspace of the balanced split, from one grid size: P pieces' partial
+// results (2 per piece: running max and sum, then G x D outputs) and, at a
+// 256-byte boundary after them, one arrival counter per segment.
+struct BalLayout {
+  int64_t P;
+  size_t counters_at, total;
+};
+BalLayout bal_layout(int B, int Hkv, int G, int D, int slots_per_seg) {
   const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
-  const int64_t P = bal_grid(N);
-  const size_t parts = static_cast<size_t>(P) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
-  const size_t counters = static_cast<size_t>(B) * Hkv * sizeof(int32_t);
-  return (parts + 255) / 256 * 256 + counters;
+  BalLayout L;
+  L.P = bal_grid(N);
+  const size_t parts = static_cast<size_t>(L.P) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
+  L.counters_at = (parts + 255) / 256 * 256;
+  L.total = L.counters_at + static_cast<size_t>(B) * Hkv * sizeof(int32_t);
+  return L;
+}
+
+size_t attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg) {
+  return bal_layout(B, Hkv, G, D, slots_per_seg).total;
+}
+
+// The balanced split on a workspace laid out as L says.
+static cudaError_t launch_bal(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
+                              const int32_t *seq_len, int B, int Hkv, int G, int D, float scale, float *out,
+                              float *lse, void *ws, const BalLayout &L, int32_t *status, cudaStream_t st) {
+  float *part = static_cast<float *>(ws);
+  int32_t *counter = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + L.counters_at);
+  if (D == 128) {
+    if (G <= 8)
+      return launch_bal_t<8, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                                counter, L.P, st);
+    return launch_bal_t<8, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                              counter, L.P, st);
+  }
+  if (G <= 8)
+    return launch_bal_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                              counter, L.P, st);
+  return launch_bal_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
+                            counter, L.P, st);
 }
 
 cudaError_t launch_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool, const int32_t *table,
                                          int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G, int D,
                                          float scale, float *out, float *lse, void *ws, int32_t *status,
                                          cudaStream_t st) {
-  const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
-  const int64_t P = bal_grid(N);
-  const size_t parts = static_cast<size_t>(P) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
-  float *part = static_cast<float *>(ws);
-  int32_t *counter = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(ws) + (parts + 255) / 256 * 256);
-  if (D == 128) {
-    if (G <= 8)
-      return launch_bal_t<8, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
-                                counter, st);
-    return launch_bal_t<8, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
-                              counter, st);
-  }
-  if (G <= 8)
-    return launch_bal_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
-                              counter, st);
-  return launch_bal_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, part,
-                            counter, st);
+  return launch_bal(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws,
+                    bal_layout(B, Hkv, G, D, slots_per_seg), status, st);
 }
 
 // ---- the balanced split without caller memory -------------------------------
@@ -827,40 +846,62 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
-// Device address of the scratch on the current device, looked up once per device.
-static void *noalloc_scratch() {
-  constexpr int kMaxDevices = 64;
-  static std::mutex mu;
-  static void *addr[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+// Identity of the current CUDA context: cuCtxGetId through the runtime's
+// driver entry points (no link to the driver library).  A device reset or a
+// released and recreated primary context is a new context with a new id.
+static bool current_context_id(unsigned long long *id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;  // none before the runtime has made one current
+  return get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch in the current context, looked up once per
+// context: the address belongs to the module loaded in that context, so a new
+// context (after a device reset, say) gets its own lookup, never a stale one.
+static void *noalloc_scratch() {
+  static std::mutex mu;
+  static std::vector<std::pair<unsigned long long, void *>> addr;  // (context id, address)
+  unsigned long long ctx = 0;
+  const bool known = current_context_id(&ctx);
+  std::lock_guard<std::mutex> lock(mu);
+  if (known)
+    for (const auto &e : addr)
+      if (e.first == ctx) return e.second;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;  // (makes the context if none)
+  if (known || current_context_id(&ctx)) addr.emplace_back(ctx, p);
+  return p;
 }
 
 cudaError_t launch_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, const int32_t *table,
                                               int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G,
                                               int D, float scale, float *out, float *lse, int32_t *status,
                                               cudaStream_t st) {
-  if (attn_workspace_bytes(B, Hkv, G, D, slots_per_seg) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  const BalLayout L = bal_layout(B, Hkv, G, D, slots_per_seg);  // one grid size for the memset and the launch
+  if (L.total > kNoAllocScratchBytes) return cudaErrorInvalidValue;
   void *ws = noalloc_scratch();
   if (ws == nullptr) return cudaErrorInvalidDevice;
   // The per-segment arrival counters must start at zero.  Every completed call
   // leaves them at zero, but one that timed out may not, so clear them on every
   // call (a memset of 4 bytes per segment, no allocation).
-  const int64_t N = static_cast<int64_t>(B) * Hkv * slots_per_seg;
-  const size_t parts = static_cast<size_t>(bal_grid(N)) * 2 * static_cast<size_t>(G) * (D + 2) * sizeof(float);
-  const size_t counters_at = (parts + 255) / 256 * 256;
-  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + counters_at, 0,
+  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(ws) + L.counters_at, 0,
                                   static_cast<size_t>(B) * Hkv * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
-  return launch_sparse_decode_attn_ws(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws,
-                                      status, st);
+  return launch_bal(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, ws, L, status, st);
 }
 
 }  // namespace oasis

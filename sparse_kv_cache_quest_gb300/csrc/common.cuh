@@ -16,6 +16,14 @@ constexpr int kBlockTokens = 16;  // tokens per logical KV block
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// max with NaN propagation (either input NaN -> NaN), as the IEEE maximum the
+// oracle's np.maximum follows; equal to fmaxf on numbers.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
 __device__ __forceinline__ void report(int32_t *status, int bits) {
   if (status != nullptr && bits != 0) atomicOr(status, bits);
 }

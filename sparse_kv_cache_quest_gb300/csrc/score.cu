@@ -5,6 +5,9 @@
 //   score[s][b] = max over the Nq = G*Nd query vectors of
 //                 sum_{d ascending, from +0, fp32 RN} q_d * (q_d >= 0 ? kmax_d : kmin_d)
 //
+// The max over the query vectors propagates NaN (as the IEEE maximum does), so
+// a NaN key or query gives a NaN score, which the selection flags.
+//
 // Exactness.  Each term is the product of two bf16 values, exact in fp32, so
 // the kernel writes the term as two fused multiply-adds,
 //     acc = fma(qn_d, kmin_d, acc);  acc = fma(qp_d, kmax_d, acc)
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kThreads) __maxnreg__(max_regs<NQP>())
           for (int jp = 0; jp < NQP / 2; ++jp) {
             float a0, a1;
             unpack2(acc[i][jp], a0, a1);
-            best = jp == 0 ? fmaxf(a0, a1) : fmaxf(best, fmaxf(a0, a1));
+            best = jp == 0 ? max_nan(a0, a1) : max_nan(best, max_nan(a0, a1));  // NaN propagates
           }
           const int b = base + lane + 32 * i;
           if (b < nc) scores[static_cast<int64_t>(s) * Nb_max + b] = best;
@@ -383,7 +386,7 @@ __global__ void __maxnreg__(128)
             for (int jp = 0; jp < kQG; ++jp) {
               float a0, a1;
               unpack2(acc[i][jp], a0, a1);
-              best[i] = fmaxf(best[i], fmaxf(a0, a1));
+              best[i] = max_nan(best[i], max_nan(a0, a1));  // NaN propagates
             }
         }
         // the next round's unit: its loads overlap this round's merge
@@ -402,7 +405,7 @@ __global__ void __maxnreg__(128)
         if (b >= ceil_div(Lu, kBlockTokens) - W) continue;
         const float *col = pm + (t / kUnit) * NG * kUnit + t % kUnit;
         float m = col[0];
-        for (int gq = 1; gq < NG; ++gq) m = fmaxf(m, col[gq * kUnit]);
+        for (int gq = 1; gq < NG; ++gq) m = max_nan(m, col[gq * kUnit]);
         scores[static_cast<int64_t>(su) * Nb_max + b] = m;
       }
       __syncthreads();  // pm is rewritten next round

@@ -143,12 +143,6 @@ __device__ __forceinline__ uint32_t neg_halves(uint32_t x) {
   asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(r) : "r"(x));
   return r;
 }
-// max with NaN propagation (either input NaN -> NaN)
-__device__ __forceinline__ float max_nan(float a, float b) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
 
 struct TileIter {
   // the CTA's tiles [t0, t1) in segment-major order; a tile is work when its

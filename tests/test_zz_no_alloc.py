@@ -66,7 +66,17 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     # 16 query heads per KV head, D = 128, 2^20 slot tiles: the workspace needs more than 8 MiB
     B, Hkv, G, D, slots = 64, 8, 16, 128, 2048
     assert okv.oasis_attn_workspace_bytes(B, Hkv, G, D, slots) > (8 << 20)
-    p = 1 << 20
+    # real buffers of the shape's sizes, every table entry empty: were the host
+    # check to let the call through, the kernel would load no tile and write zeros
+    q = torch.zeros((B, Hkv * G, D), dtype=torch.bfloat16, device=DEV)
+    table = torch.full((B * Hkv, slots), -1, dtype=torch.int32, device=DEV)
+    pool = torch.zeros((1, 1, 2, 16, D), dtype=torch.bfloat16, device=DEV)
+    lens = torch.full((B,), 16 * slots, dtype=torch.int32, device=DEV)
+    out = torch.empty((B, Hkv * G, D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((B, Hkv * G), dtype=torch.float32, device=DEV)
+    st = torch.zeros((1,), dtype=torch.int32, device=DEV)
     with pytest.raises(ob.OasisError) as e:
-        okv.oasis_sparse_decode_attn_noalloc(p, p, p, slots, p, B, Hkv, G, D, 0.1, p)
+        okv.oasis_sparse_decode_attn_noalloc(q, pool, table, slots, lens, B, Hkv, G, D, 0.1, out, lse, st)
     assert e.value.code == ob.EINVAL
+    torch.cuda.synchronize()
+    assert st.item() == 0
