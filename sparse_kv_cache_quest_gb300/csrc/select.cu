@@ -18,9 +18,9 @@
 // One CTA of 512 threads per segment, everything in shared memory:
 //  * scores -> order-preserving 32-bit keys (larger key = larger score; -0 is
 //    mapped to +0 so the two tie; NaN maps to 0, below -inf, and is flagged);
-//  * T by a 4-pass 8-bit MSB radix select of the K-th largest key (warp-
-//    aggregated shared-memory histograms), then ties at the threshold taken in
-//    ascending block order through a block-wide prefix count;
+//  * T by a 4-pass 8-bit MSB radix select of the K-th largest key (shared-
+//    memory histograms, the digit of each pass found by one warp), then ties
+//    at the threshold taken in ascending block order;
 //  * T, R as bitmaps; the small lists T\R and R\T are ranked by counting
 //    (O(n^2) over <= K entries, no sorting network, few barriers) with the
 //    unique 64-bit composite key (key << 32) | ~block.
@@ -41,6 +41,11 @@ __device__ __forceinline__ uint32_t score_key(float f, bool &nan) {
   }
   if (u == 0x80000000u) u = 0u;  // -0 ties with +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The score a key came from (NaN for the key of a NaN; +0 for the key of -0).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 __device__ __forceinline__ uint64_t composite(uint32_t key, int b) {
@@ -82,12 +87,13 @@ __device__ int block_exclusive_scan(int v, int *warp_tot) {
 struct SelScalars {
   int err;
   int nN, nE, nF, nEmpty;
-  uint32_t digit;
+  uint32_t digit, dcount;  // radix select: the pass's digit and the keys in its bin
   int remaining;
   int warp_tot[kWarps];
 };
 
-static_assert(sizeof(SelScalars) + 3 * 256 * sizeof(uint32_t) <= kStaticSmemBound, "static shared memory bound");
+static_assert(sizeof(SelScalars) + 2 * 256 * sizeof(uint32_t) + 4 * kWarps * sizeof(float) + 64 <= kStaticSmemBound,
+              "static shared memory bound");
 
 // Sum of v over the CTA (all threads call it, all get the sum).
 __device__ int block_sum(int v, int *warp_tot) {
@@ -103,41 +109,48 @@ __device__ int block_sum(int v, int *warp_tot) {
   return t;
 }
 
-// T as a bitmap: the first min(K, nc) candidates by (key desc, block asc).
-// 4-pass 8-bit MSB radix select of the K-th largest key (warp-aggregated
-// shared-memory histograms, triple-buffered so each pass takes one barrier),
-// then the keys equal to it taken in ascending block order through a
-// block-wide prefix count.  bmT must be clear; all threads call it; the caller
-// synchronises before reading bmT.
+// T as a bitmap: min(K, nc) candidates, the first by (key desc, block asc)
+// when PASSES = 4.  An MSB radix select over the top 8 * PASSES bits of the
+// keys finds the bin b* holding the K-th largest key (per pass: the keys
+// matching the prefix so far counted into a 256-bin shared histogram with
+// plain shared atomics, the bin found by one warp and published through shared
+// memory); T = the keys above b* and the first keys of b* in ascending block
+// order, all of b* (one ballot per bitmap word) when it holds no more keys
+// than are still needed, else through a block-wide prefix count.  With
+// PASSES = 4 the bin is one key value and T is exact; with fewer passes T is
+// exact up to the order inside the last bin (PASSES = 3: keys within 2^8 units
+// in the last place of each other), which the certified selection accepts (it
+// settles any K candidates).  bmT must be clear and hist[0] zero; all threads
+// call it; the caller synchronises before reading bmT.
+template <int PASSES>
 __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, uint32_t (*hist)[256],
                             SelScalars &sc) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (nc <= K) {
-    for (int b = tid; b < nc; b += kThreads) atomicOr(&bmT[b >> 5], 1u << (b & 31));
-  } else {
-    uint32_t prefix = 0u, pmask = 0u;
-    int remaining = K;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      uint32_t *h = hist[pass % 3];
-      for (int i = tid; i < 256; i += kThreads) hist[(pass + 1) % 3][i] = 0u;
-      for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
-        const int b = b0 + lane;
-        int dig = -1;
-        if (b < nc) {
-          const uint32_t key = keys[b];
-          if ((key & pmask) == prefix) dig = static_cast<int>((key >> shift) & 0xFFu);
-        }
-        const unsigned grp = __match_any_sync(0xFFFFFFFFu, dig);
-        if (dig >= 0 && lane == __ffs(grp) - 1) atomicAdd(&h[dig], static_cast<uint32_t>(__popc(grp)));
-      }
-      // The only barrier of the pass: the counts are complete, the next buffer is
-      // clear, and every warp has finished reading the buffer cleared next pass.
-      __syncthreads();
-      // Every warp finds the digit of the remaining-th largest key on its own.
-      // Lane l owns bins 255-8l down to 248-8l (descending digit order).
-      // (two 16-byte loads per lane: consecutive lanes read consecutive 16-byte
-      // chunks, so every warp's reads are free of bank conflicts)
+    for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, b0 + lane < nc);
+      if (lane == 0) bmT[b0 >> 5] = m;
+    }
+    return;
+  }
+  uint32_t prefix = 0u, pmask = 0u, bin_count = 0u;
+  int remaining = K;
+  for (int pass = 0; pass < PASSES; ++pass) {
+    const int shift = 24 - 8 * pass;
+    uint32_t *h = hist[pass & 1];
+    // four keys loaded before their atomics (independent loads in flight)
+    for (int b0 = tid; b0 < nc; b0 += 4 * kThreads) {
+      uint32_t k4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) k4[u] = b0 + u * kThreads < nc ? keys[b0 + u * kThreads] : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (b0 + u * kThreads < nc && (k4[u] & pmask) == prefix) atomicAdd(&h[(k4[u] >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // the bin of the remaining-th largest key; lane l owns bins 255-8l down to
+      // 248-8l (two 16-byte loads per lane, consecutive lanes consecutive chunks)
       const uint4 lo4 = reinterpret_cast<const uint4 *>(h)[62 - 2 * lane];  // bins 248-8l .. 251-8l
       const uint4 hi4 = reinterpret_cast<const uint4 *>(h)[63 - 2 * lane];  // bins 252-8l .. 255-8l
       const uint32_t c[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
@@ -150,45 +163,53 @@ __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, 
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += y;
       }
-      const uint32_t before = incl - sum;
-      uint32_t digit = 0u;
-      int rem = 0;
-      const bool mine = before < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl;
-      if (mine) {
+      const uint32_t before = incl - sum, want = static_cast<uint32_t>(remaining);
+      if (before < want && want <= incl) {  // exactly one lane
         uint32_t cum = before;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          if (cum < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= cum + c[q]) {
-            digit = static_cast<uint32_t>(255 - 8 * lane - q);
-            rem = remaining - static_cast<int>(cum);
+          if (cum < want && want <= cum + c[q]) {
+            sc.digit = static_cast<uint32_t>(255 - 8 * lane - q);
+            sc.remaining = static_cast<int>(want - cum);
+            sc.dcount = c[q];
           }
           cum += c[q];
         }
       }
-      const unsigned holders = __ballot_sync(0xFFFFFFFFu, mine);  // exactly one lane holds it
-      const int src = holders ? __ffs(holders) - 1 : 0;
-      digit = __shfl_sync(0xFFFFFFFFu, digit, src);
-      rem = __shfl_sync(0xFFFFFFFFu, rem, src);
-      prefix |= digit << shift;
-      pmask |= 0xFFu << shift;
-      remaining = rem;
+      // the other histogram is counted into next pass: clear it (its last
+      // reader, this warp, finished a barrier ago)
+      uint4 *nh = reinterpret_cast<uint4 *>(hist[(pass + 1) & 1]);
+      nh[2 * lane] = make_uint4(0u, 0u, 0u, 0u);
+      nh[2 * lane + 1] = make_uint4(0u, 0u, 0u, 0u);
     }
-    const uint32_t tau = prefix;
-    const int need = remaining;  // keys equal to tau to take, lowest block id first
-    const int per = ceil_div(nc, kThreads);
-    const int lo = min(nc, tid * per), hi = min(nc, lo + per);
-    int ties = 0;
-    for (int b = lo; b < hi; ++b) ties += keys[b] == tau;
-    int before = block_exclusive_scan(ties, sc.warp_tot);
-    for (int b = lo; b < hi; ++b) {
-      const uint32_t key = keys[b];
-      bool in = key > tau;
-      if (key == tau) {
-        in = before < need;
-        ++before;
-      }
-      if (in) atomicOr(&bmT[b >> 5], 1u << (b & 31));
+    __syncthreads();
+    prefix |= sc.digit << shift;
+    pmask |= 0xFFu << shift;
+    remaining = sc.remaining;
+    bin_count = sc.dcount;
+  }
+  const int need = remaining;  // keys of the last bin to take, lowest block id first
+  if (static_cast<uint32_t>(need) == bin_count) {
+    for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
+      const int b = b0 + lane;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, b < nc && (keys[b] & pmask) >= prefix);
+      if (lane == 0) bmT[b0 >> 5] = m;
     }
+    return;
+  }
+  const int per = ceil_div(nc, kThreads);
+  const int lo = min(nc, tid * per), hi = min(nc, lo + per);
+  int ties = 0;
+  for (int b = lo; b < hi; ++b) ties += (keys[b] & pmask) == prefix;
+  int before = block_exclusive_scan(ties, sc.warp_tot);
+  for (int b = lo; b < hi; ++b) {
+    const uint32_t km = keys[b] & pmask;
+    bool in = km > prefix;
+    if (km == prefix) {
+      in = before < need;
+      ++before;
+    }
+    if (in) atomicOr(&bmT[b >> 5], 1u << (b & 31));
   }
 }
 
@@ -212,7 +233,7 @@ constexpr int kBatch = 32;  // blocks recomputed per pass
 // of the dynamic allocation; one definition serves the kernel's pointers and
 // the launcher's allocation size.
 struct CertLayout {
-  size_t stage, qsm, res, bmX, xl, rankE, end;
+  size_t stage, qsm, res, bmX, xl, rankE, rad, end;
 };
 __host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max, int K, int CH, int Nq) {
   const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
@@ -224,7 +245,8 @@ __host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max,
   L.bmX = L.res + 4 * static_cast<size_t>(kBatch) * Nq4;                 // float [kBatch][Nq4]
   L.xl = L.bmX + 4 * words;                                              // uint32 [words]
   L.rankE = L.xl + 4 * static_cast<size_t>(Nb_max);                      // int32 [Nb_max]
-  L.end = L.rankE + 4 * static_cast<size_t>(K);                          // int32 [K]
+  L.rad = L.rankE + 4 * static_cast<size_t>(K);                          // int32 [K]
+  L.end = L.rad + 4 * static_cast<size_t>(Nb_max);                       // float [Nb_max]
   return L;
 }
 
@@ -235,35 +257,52 @@ struct CertArgs {
   int G, Nd;
 };
 
-__device__ float block_reduce(float v, bool is_max, float *red) {
+// CTA-wide min of each lo[k] and max of each hi[k] (NaN ignored), one
+// barrier pair for all of them; every thread gets the results.
+template <int N>
+__device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float y = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    v = is_max ? fmaxf(v, y) : fminf(v, y);
+  for (int k = 0; k < N; ++k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo[k] = fminf(lo[k], __shfl_xor_sync(0xFFFFFFFFu, lo[k], o));
+      hi[k] = fmaxf(hi[k], __shfl_xor_sync(0xFFFFFFFFu, hi[k], o));
+    }
   }
   __syncthreads();  // red may still be read by a previous reduction
-  if (lane == 0) red[warp] = v;
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      red[2 * k][warp] = lo[k];
+      red[2 * k + 1][warp] = hi[k];
+    }
+  }
   __syncthreads();
-  float r = red[0];
-  for (int w = 1; w < kWarps; ++w) r = is_max ? fmaxf(r, red[w]) : fminf(r, red[w]);
-  return r;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    for (int w = 0; w < kWarps; ++w) {
+      lo[k] = fminf(lo[k], red[2 * k][w]);
+      hi[k] = fmaxf(hi[k], red[2 * k + 1][w]);
+    }
+  }
 }
 
 // Fixed-order fp32 scores of the listed blocks (the oasis_score_blocks
 // arithmetic: per query, sum over d ascending from +0 of q_d * (q_d >= 0 ?
 // kmax_d : kmin_d), one rounding per term; max over the queries, NaN kept).
-// Writes them to srow and their keys to keys, marks them in bmX.
-// A thread takes one block and four queries (the widened summary values serve
-// all four); qsm holds the queries as [d][Nq4], Nq4 = Nq rounded up to 4, the
-// padding repeating the last query.
+// Writes them to srow and their keys to keys, zeroes their radii in rad (a
+// recomputed score is exact), marks them in bmX.  A thread takes one (block,
+// query) pair at a time; qsm holds the queries as [d][Nq4].  The max over a
+// block's queries is taken by one warp as the largest order key of the sums
+// (+0 above -0), which does not depend on the order of the reduction.
 template <int CH>
 __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
                                  int Nq, const float *qsm, uint4 *stage, float *res, float *srow, uint32_t *keys,
-                                 uint32_t *bmX, SelScalars &sc) {
+                                 float *rad, uint32_t *bmX, SelScalars &sc) {
   constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
-  const int tid = threadIdx.x;
-  const int Nq4 = (Nq + 3) & ~3, ng = Nq4 / 4;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Nq4 = (Nq + 3) & ~3;
   for (int e0 = 0; e0 < n; e0 += kBatch) {
     const int nb = min(kBatch, n - e0);
     for (int i = tid; i < nb * 2 * CH; i += kThreads) {
@@ -272,12 +311,12 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
       stage[e * ES + k] = __ldg((k < CH ? gmin : gmax) + static_cast<int64_t>(c) * Nb_max + b);
     }
     __syncthreads();
-    for (int i = tid; i < nb * ng; i += kThreads) {
-      const int e = i / ng, g = i % ng;
+    for (int i = tid; i < nb * Nq; i += kThreads) {
+      const int e = i / Nq, j = i - e * Nq;
       const uint4 *st = stage + e * ES;
-      const float *qg = qsm + 4 * g;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
+      const float *qj = qsm + j;
+      float acc = 0.0f;
+#pragma unroll 2
       for (int c = 0; c < CH; ++c) {
         const uint4 mn = st[c], mx = st[CH + c];
         const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w}, wx[4] = {mx.x, mx.y, mx.z, mx.w};
@@ -285,42 +324,43 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
         for (int t = 0; t < 8; ++t) {
           const float kn = (t & 1) ? bf16_hi(wn[t >> 1]) : bf16_lo(wn[t >> 1]);
           const float kx = (t & 1) ? bf16_hi(wx[t >> 1]) : bf16_lo(wx[t >> 1]);
-          const float4 q = *reinterpret_cast<const float4 *>(qg + (c * 8 + t) * Nq4);
-          acc[0] = fmaf(q.x, q.x >= 0.0f ? kx : kn, acc[0]);  // exact product, one rounding
-          acc[1] = fmaf(q.y, q.y >= 0.0f ? kx : kn, acc[1]);
-          acc[2] = fmaf(q.z, q.z >= 0.0f ? kx : kn, acc[2]);
-          acc[3] = fmaf(q.w, q.w >= 0.0f ? kx : kn, acc[3]);
+          const float q = qj[(c * 8 + t) * Nq4];
+          acc = fmaf(q, q >= 0.0f ? kx : kn, acc);  // exact product, one rounding
         }
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) res[e * Nq4 + 4 * g + k] = acc[k];
+      res[e * Nq4 + j] = acc;
     }
     __syncthreads();
-    for (int e = tid; e < nb; e += kThreads) {
-      float best = -INFINITY;
+    for (int e = warp; e < nb; e += kWarps) {
+      uint32_t best = 0u;  // below the order key of every non-NaN float
       bool nan = false;
-      for (int j = 0; j < Nq; ++j) {
-        const float v = res[e * Nq4 + j];
-        nan |= v != v;
-        best = fmaxf(best, v);
+      for (int j = lane; j < Nq; j += 32) {
+        const uint32_t u = __float_as_uint(res[e * Nq4 + j]);
+        nan |= (u & 0x7FFFFFFFu) > 0x7F800000u;
+        best = max(best, (u & 0x80000000u) ? ~u : (u | 0x80000000u));
       }
-      const float v = nan ? __uint_as_float(0x7FC00000u) : best;
-      const int b = xl[e0 + e];
-      srow[b] = v;
-      bool isn = false;
-      keys[b] = score_key(v, isn);
-      if (isn) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
-      atomicOr(&bmX[b >> 5], 1u << (b & 31));
+      best = __reduce_max_sync(0xFFFFFFFFu, best);
+      nan = __any_sync(0xFFFFFFFFu, nan);
+      if (lane == 0) {
+        const float v = nan ? __uint_as_float(0x7FC00000u)
+                            : __uint_as_float((best & 0x80000000u) ? (best & 0x7FFFFFFFu) : ~best);
+        const int b = xl[e0 + e];
+        srow[b] = v;
+        bool isn = false;
+        keys[b] = score_key(v, isn);
+        rad[b] = 0.0f;
+        if (isn) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
+        atomicOr(&bmX[b >> 5], 1u << (b & 31));
+      }
     }
     __syncthreads();
   }
 }
 
-// interval of block b: recomputed blocks are exact (radius 0)
-__device__ __forceinline__ void interval(const float *srow, const float *rrow, const uint32_t *bmX, int b, float &lo,
-                                         float &hi) {
-  const float v = srow[b];
-  const float r = bit(bmX, b) ? 0.0f : rrow[b];
+// interval of block b from its key and radius (a recomputed block has radius 0)
+__device__ __forceinline__ void interval(const uint32_t *keys, const float *rad, int b, float &lo, float &hi) {
+  const float v = key_score(keys[b]);
+  const float r = rad[b];
   lo = v - r;
   hi = v + r;
 }
@@ -336,8 +376,8 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
                                                      int32_t *status, CertArgs ca) {
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ SelScalars sc;
-  __shared__ __align__(16) uint32_t hist[3][256];  // pass p counts into hist[p % 3], clears hist[(p + 1) % 3]
-  __shared__ float red[kWarps];
+  __shared__ __align__(16) uint32_t hist[2][256];  // radix pass p counts into hist[p & 1]
+  __shared__ float red[4][kWarps];
   __shared__ int nX;
 
   const int s = blockIdx.x;
@@ -356,10 +396,9 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   int32_t *aSorted = rankN + K;                                // [cap]
   int32_t *fList = aSorted + cap;                              // [cap]
   int32_t *fSorted = fList + cap;                              // [cap]
-  // certified selection only (sized by cert_smem_bytes)
+  // certified selection only (laid out by cert_layout, which the launcher sizes with)
   constexpr int D = CH * 8;
   const int Nq = CERTIFY ? ca.G * ca.Nd : 0;
-  const int Nq4 = (Nq + 3) & ~3;
   const CertLayout cl = cert_layout(reinterpret_cast<unsigned char *>(fSorted + cap) - smraw, Nb_max, K, CH, Nq);
   uint4 *stage = reinterpret_cast<uint4 *>(smraw + cl.stage);      // staged summaries of recomputed blocks
   float *qsm = reinterpret_cast<float *>(smraw + cl.qsm);          // [D][Nq4] queries
@@ -367,6 +406,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   uint32_t *bmX = reinterpret_cast<uint32_t *>(smraw + cl.bmX);    // [words] recomputed blocks
   int32_t *xl = reinterpret_cast<int32_t *>(smraw + cl.xl);        // [Nb_max] blocks to recompute
   int32_t *rankE = reinterpret_cast<int32_t *>(smraw + cl.rankE);  // [K]
+  float *rad = reinterpret_cast<float *>(smraw + cl.rad);          // [Nb_max] radii, 0 once recomputed
   float *srow_w = CERTIFY ? ca.scores + static_cast<int64_t>(s) * Nb_max : nullptr;
   const float *rrow = CERTIFY ? ca.radius + static_cast<int64_t>(s) * Nb_max : nullptr;
   const uint4 *gmin = CERTIFY ? reinterpret_cast<const uint4 *>(ca.kmin) + static_cast<int64_t>(s) * CH * Nb_max
@@ -393,8 +433,9 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
     // the segment's query vectors, widened: qsm[d][j], j = draft * G + head in group,
     // padded to a multiple of 4 by repeating the last one
     const int Hq = Hkv * ca.G, bseq = s / Hkv, h = s % Hkv, Nq4 = (Nq + 3) & ~3;
+    // (consecutive threads take consecutive queries: the stores are free of bank conflicts)
     for (int i = tid; i < Nq4 * CH; i += kThreads) {
-      const int j = i / CH, c = i % CH, jq = min(j, Nq - 1), jd = jq / ca.G, g = jq % ca.G;
+      const int j = i % Nq4, c = i / Nq4, jq = min(j, Nq - 1), jd = jq / ca.G, g = jq % ca.G;
       const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
           ca.qdraft + ((static_cast<int64_t>(bseq) * ca.Nd + jd) * Hq + h * ca.G + g) * D + c * 8));
       const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -405,6 +446,8 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   bool nan = false;
   const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
   for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
+  if constexpr (CERTIFY)
+    for (int b = tid; b < nc; b += kThreads) rad[b] = rrow[b];
   __syncthreads();
   if (nan) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
 
@@ -436,29 +479,27 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   if constexpr (CERTIFY) {
     if (nc > K) {
       // T by the estimates, then the blocks it cannot settle
-      topk_bitmap(keys, nc, K, bmT, hist, sc);
+      topk_bitmap<3>(keys, nc, K, bmT, hist, sc);
       __syncthreads();
-      float lo_in = INFINITY, hi_out = -INFINITY;
+      float lo_in[1] = {INFINITY}, hi_out[1] = {-INFINITY};
       for (int b = tid; b < nc; b += kThreads) {
         float lo, hi;
-        interval(srow, rrow, bmX, b, lo, hi);
+        interval(keys, rad, b, lo, hi);
         if (lo != lo || hi != hi) continue;  // NaN estimate: recomputed below
         if (bit(bmT, b))
-          lo_in = fminf(lo_in, lo);
+          lo_in[0] = fminf(lo_in[0], lo);
         else
-          hi_out = fmaxf(hi_out, hi);
+          hi_out[0] = fmaxf(hi_out[0], hi);
       }
-      lo_in = block_reduce(lo_in, false, red);
-      hi_out = block_reduce(hi_out, true, red);
-      if (tid == 0) nX = 0;
-      __syncthreads();
+      if (tid == 0) nX = 0;  // read after the reduction's barriers
+      block_minmax<1>(lo_in, hi_out, red);
       for (int b = tid; b < nc; b += kThreads) {
         float lo, hi;
-        interval(srow, rrow, bmX, b, lo, hi);
-        if (!(lo > hi_out) && !(hi < lo_in)) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
+        interval(keys, rad, b, lo, hi);
+        if (!(lo > hi_out[0]) && !(hi < lo_in[0])) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, rad, bmX, sc);
       // T = the settled members of the estimated T, and as many of the recomputed
       // ones as the estimated T held, best first by the exact keys
       int need = 0;
@@ -483,12 +524,12 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       __syncthreads();
     }
   } else {
-    topk_bitmap(keys, nc, K, bmT, hist, sc);
+    topk_bitmap<4>(keys, nc, K, bmT, hist, sc);
     __syncthreads();
   }
   if constexpr (CERTIFY) {
     if (nc <= K) {
-      topk_bitmap(keys, nc, K, bmT, hist, sc);  // every candidate
+      topk_bitmap<4>(keys, nc, K, bmT, hist, sc);  // every candidate
       __syncthreads();
     }
   }
@@ -540,43 +581,42 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
         if (lane == 0) rankE[i] = r;
       }
       __syncthreads();
-      float a_lo = INFINITY, a_hi = -INFINITY, e_lo = INFINITY, e_hi = -INFINITY;
+      // lo[0]/hi[0]: min over A~ / max over N \ A~; lo[1]/hi[1]: min over the kept
+      // of E / max over the evicted of E
+      float lo_[2] = {INFINITY, INFINITY}, hi_[2] = {-INFINITY, -INFINITY};
       for (int i = tid; i < nN; i += kThreads) {
         float lo, hi;
-        interval(srow, rrow, bmX, composite_block(listN[i]), lo, hi);
+        interval(keys, rad, composite_block(listN[i]), lo, hi);
         if (rankN[i] < nA)
-          a_lo = fminf(a_lo, lo);
+          lo_[0] = fminf(lo_[0], lo);
         else
-          a_hi = fmaxf(a_hi, hi);
+          hi_[0] = fmaxf(hi_[0], hi);
       }
       for (int i = tid; i < nE; i += kThreads) {
         float lo, hi;
-        interval(srow, rrow, bmX, composite_block(listE[i]), lo, hi);
+        interval(keys, rad, composite_block(listE[i]), lo, hi);
         if (rankE[i] < nEvict)
-          e_hi = fmaxf(e_hi, hi);  // evicted by the estimates
+          hi_[1] = fmaxf(hi_[1], hi);  // evicted by the estimates
         else
-          e_lo = fminf(e_lo, lo);  // kept by the estimates
+          lo_[1] = fminf(lo_[1], lo);  // kept by the estimates
       }
-      a_lo = block_reduce(a_lo, false, red);
-      a_hi = block_reduce(a_hi, true, red);
-      e_lo = block_reduce(e_lo, false, red);
-      e_hi = block_reduce(e_hi, true, red);
-      if (tid == 0) nX = 0;
-      __syncthreads();
+      if (tid == 0) nX = 0;  // read after the reduction's barriers
+      block_minmax<2>(lo_, hi_, red);
+      const float a_lo = lo_[0], a_hi = hi_[0], e_lo = lo_[1], e_hi = hi_[1];
       for (int i = tid; i < nN && certA; i += kThreads) {
         const int b = composite_block(listN[i]);
         float lo, hi;
-        interval(srow, rrow, bmX, b, lo, hi);
+        interval(keys, rad, b, lo, hi);
         if (!bit(bmX, b) && !(lo > a_hi) && !(hi < a_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       for (int i = tid; i < nE && certE; i += kThreads) {
         const int b = composite_block(listE[i]);
         float lo, hi;
-        interval(srow, rrow, bmX, b, lo, hi);
+        interval(keys, rad, b, lo, hi);
         if (!bit(bmX, b) && !(lo > e_hi) && !(hi < e_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, rad, bmX, sc);
       for (int i = tid; i < nN; i += kThreads) {
         const int b = composite_block(listN[i]);
         listN[i] = composite(keys[b], b);
