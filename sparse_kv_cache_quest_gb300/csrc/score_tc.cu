@@ -150,13 +150,18 @@ struct TileIter {
   int64_t t0, t1;
   int tps, Hkv, W, Nb_max;
   const int32_t *seq_len;
-  __device__ int nc_of(int s) const {
-    int L = __ldg(seq_len + s / Hkv);
-    L = L < 0 ? 0 : (L > Nb_max * kBlockTokens ? Nb_max * kBlockTokens : L);
-    return ceil_div(L, kBlockTokens) - W;
+  int s_last = -1, nc_last = 0;  // the last segment asked about (a load per segment, not per tile)
+  __device__ int nc_of(int s) {
+    if (s != s_last) {
+      int L = __ldg(seq_len + s / Hkv);
+      L = L < 0 ? 0 : (L > Nb_max * kBlockTokens ? Nb_max * kBlockTokens : L);
+      s_last = s;
+      nc_last = ceil_div(L, kBlockTokens) - W;
+    }
+    return nc_last;
   }
   // first work tile at or after t (t1 if none); nc of its segment in *nc
-  __device__ int64_t next(int64_t t, int *nc) const {
+  __device__ int64_t next(int64_t t, int *nc) {
     while (t < t1) {
       const int s = static_cast<int>(t / tps);
       const int n = nc_of(s);
@@ -170,7 +175,7 @@ struct TileIter {
     return t1;
   }
   // does segment s have a work tile in [t0, t1)?
-  __device__ bool active(int s) const {
+  __device__ bool active(int s) {
     const int64_t first = std::max<int64_t>(t0, static_cast<int64_t>(s) * tps);
     return static_cast<int>(first - static_cast<int64_t>(s) * tps) * kRows < nc_of(s);
   }
@@ -196,7 +201,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   float *sQmax = sC + kNC * kRows;                                  // [2]: max_d Q_d per query buffer
   uint64_t *bars = reinterpret_cast<uint64_t *>(sQmax + 2);
   uint64_t *full = bars, *empty = full + stages, *accF = empty + stages, *accE = accF + kNAcc;
-  uint64_t *bqF = accE + kNAcc, *bqE = bqF + 2, *cF = bqE + 2, *cE = cF + kNC, *drain = cE + kNC;
+  uint64_t *bqF = accE + kNAcc, *bqE = bqF + 2, *qmF = bqE + 2, *qmE = qmF + 2, *cF = qmE + 2, *cE = cF + kNC;
+  uint64_t *drain = cE + kNC;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -225,6 +231,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bqF[i], 32 * kGroupWarps);
       mbar_init(&bqE[i], 1);
+      mbar_init(&qmF[i], 1);            // max_d Q_d of the buffer's segment is in sQmax
+      mbar_init(&qmE[i], kGroupWarps);  // every TMEM warp has taken it
     }
     for (int i = 0; i < kNC; ++i) {
       mbar_init(&cF[i], 32 * kGroupWarps);
@@ -375,7 +383,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       }
       // the MMAs of the segment two back (same buffer) have completed (after an
       // abort the wait returns at once; the outputs are then void anyway)
-      if (built >= 2) wait_or_abort(&bqE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
+      if (built >= 2) {
+        wait_or_abort(&bqE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
+        wait_or_abort(&qmE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
+      }
       scan_barrier();  // every scan thread is done with this buffer's previous segment
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {
@@ -414,6 +425,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         float qm = 0.0f;
         for (int d = 0; d < D; ++d) qm = fmaxf(qm, Q[d]);
         sQmax[bq] = qm;
+        mbar_arrive(&qmF[bq]);
       }
       scan_barrier();
       ++next_build;
@@ -421,88 +433,106 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     };
     build_next();
     build_next();
-    // The group never leaves this loop early: after an abort every wait returns
+    // The group never leaves these loops early: after an abort every wait returns
     // at once and the work is skipped, so all four warps meet at the same named
     // barriers (inside build_next) whatever happened.
-    int64_t i = 0, u = 0;  // tiles, half-tiles
-    int seg_prev = -1, used = 0, bq = 0;
-    int nc = 0;
-    for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
-      const int s = static_cast<int>(t / tps);
-      if (s != seg_prev) {
-        if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is rebuilt for the next-but-one
-        bq = used & 1;
-        ++used;
-        seg_prev = s;
-      }
-      const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
-      const int rows = min(kRows, nc - base);
-      // C_b: the summary values on the wrong side of zero, weighted by Q_d (kmax
-      // half: |kmax| where kmax < 0; kmin half: kmin where kmin > 0).  With wsum
-      // (their per-block sum, kept by the summary build) C_b <= max_d Q_d * wsum
-      // and the stages are not read here.
-      float C = 0.0f;
-      if (wsum != nullptr) {
-        if (row < rows) C = sQmax[bq] * __ldg(wsum + static_cast<int64_t>(s) * Nb_max + base + row);
-      } else {
+    if (wsum != nullptr) {
+      // C_b <= max_d Q_d * wsum_b is formed by the TMEM warps themselves, so this
+      // group only builds the active segments' query operands in turn (each build
+      // waits until its buffer's previous segment is done with it)
+      while (next_build <= s_last) build_next();
+    } else {
+      int64_t i = 0, u = 0;  // tiles, half-tiles
+      int seg_prev = -1, used = 0, bq = 0;
+      int nc = 0;
+      for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
+        const int s = static_cast<int>(t / tps);
+        if (s != seg_prev) {
+          if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is rebuilt for the next-but-one
+          bq = used & 1;
+          ++used;
+          seg_prev = s;
+        }
+        const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
+        const int rows = min(kRows, nc - base);
+        // C_b: the summary values on the wrong side of zero, weighted by Q_d (kmax
+        // half: |kmax| where kmax < 0; kmin half: kmin where kmin > 0), from the stages
+        float C = 0.0f;
+        {
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          const int st = static_cast<int>(u % stages);
-          const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u,
-                                                                 abort_flag));
-          if (got && row < rows) {
-            const uint8_t *A = sA + static_cast<size_t>(st) * kHalf + row * 16;
-            // fast test: any sign bit set among the kmax half (h = 0) / any clear among
-            // the kmin half (h = 1)?  (-0 and +0 pass it too; their magnitude is 0)
-            uint32_t acc_or = 0u, acc_and = 0xFFFFFFFFu;
+          for (int h = 0; h < 2; ++h) {
+            const int st = static_cast<int>(u % stages);
+            const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u,
+                                                                   abort_flag));
+            if (got && row < rows) {
+              const uint8_t *A = sA + static_cast<size_t>(st) * kHalf + row * 16;
+              // fast test: any sign bit set among the kmax half (h = 0) / any clear among
+              // the kmin half (h = 1)?  (-0 and +0 pass it too; their magnitude is 0)
+              uint32_t acc_or = 0u, acc_and = 0xFFFFFFFFu;
 #pragma unroll 8
-            for (int c = 0; c < CH; ++c) {
-              const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
-              acc_or |= x.x | x.y | x.z | x.w;
-              acc_and &= x.x & x.y & x.z & x.w;
-            }
-            const bool wrong = h == 0 ? (acc_or & 0x80008000u) != 0u : (acc_and & 0x80008000u) != 0x80008000u;
-            if (wrong) {  // the exact weighted sum
-              const float *Q = sQ + bq * D;
               for (int c = 0; c < CH; ++c) {
                 const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                acc_or |= x.x | x.y | x.z | x.w;
+                acc_and &= x.x & x.y & x.z & x.w;
+              }
+              const bool wrong = h == 0 ? (acc_or & 0x80008000u) != 0u : (acc_and & 0x80008000u) != 0x80008000u;
+              if (wrong) {  // the exact weighted sum
+                const float *Q = sQ + bq * D;
+                for (int c = 0; c < CH; ++c) {
+                  const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
+                  const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const uint32_t m = neg_halves(xs[e]);
-                  const uint32_t cw = h == 0 ? (xs[e] & m & 0x7FFF7FFFu) : (xs[e] & ~m);
-                  C = fmaf(Q[c * 8 + 2 * e], bf16_lo(cw), C);
-                  C = fmaf(Q[c * 8 + 2 * e + 1], bf16_hi(cw), C);
+                  for (int e = 0; e < 4; ++e) {
+                    const uint32_t m = neg_halves(xs[e]);
+                    const uint32_t cw = h == 0 ? (xs[e] & m & 0x7FFF7FFFu) : (xs[e] & ~m);
+                    C = fmaf(Q[c * 8 + 2 * e], bf16_lo(cw), C);
+                    C = fmaf(Q[c * 8 + 2 * e + 1], bf16_hi(cw), C);
+                  }
                 }
               }
             }
+            __syncwarp();
+            if (got && lane == 0) mbar_arrive(&empty[st]);
+            ++u;
           }
-          __syncwarp();
-          if (got && lane == 0) mbar_arrive(&empty[st]);
-          ++u;
         }
+        const int cb = static_cast<int>(i % kNC);
+        const bool room = i < kNC || __all_sync(0xFFFFFFFFu, wait_or_abort(&cE[cb], static_cast<uint32_t>((i / kNC) - 1) &
+                                                                                       1u, abort_flag));
+        if (room) {
+          sC[cb * kRows + row] = C;
+          mbar_arrive(&cF[cb]);
+        }
+        ++i;
       }
-      const int cb = static_cast<int>(i % kNC);
-      const bool room = i < kNC || __all_sync(0xFFFFFFFFu, wait_or_abort(&cE[cb], static_cast<uint32_t>((i / kNC) - 1) &
-                                                                                     1u, abort_flag));
-      if (room) {
-        sC[cb * kRows + row] = C;
-        mbar_arrive(&cF[cb]);
-      }
-      ++i;
     }
   } else {
     // ---------------- TMEM warps: accumulator row -> max -> radius -> stores
     const int quad = warp & 3;                 // the TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     int64_t i = 0;
-    int nc = 0;
+    int nc = 0, seg_cur = -1, used = 0;
+    float qmax = 0.0f;  // max_d Q_d of the current segment
     const float gamma = 0x1p-12f, floor_r = 0x1p-110f;
     for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
       const int s = static_cast<int>(t / tps);
       const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
       const int rows = min(kRows, nc - base);
       const int acc = static_cast<int>(i % kNAcc);
+      if (s != seg_cur) {  // take the segment's max_d Q_d and free its slot
+        const int b = used & 1;
+        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&qmF[b], static_cast<uint32_t>(used >> 1) & 1u, abort_flag)))
+          break;
+        qmax = sQmax[b];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&qmE[b]);
+        ++used;
+        seg_cur = s;
+      }
+      // this row's wrong-side sum, loaded before the accumulator wait so that the
+      // wait hides its latency
+      const float ws = wsum != nullptr && row < rows ? __ldg(wsum + static_cast<int64_t>(s) * Nb_max + base + row)
+                                                     : 0.0f;
       if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&accF[acc], static_cast<uint32_t>(i / kNAcc) & 1u, abort_flag)))
         break;  // the whole warp leaves together
       tc_fence_after();
@@ -522,11 +552,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accE[acc]);
-      const int cb = static_cast<int>(i % kNC);
-      if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&cF[cb], static_cast<uint32_t>(i / kNC) & 1u, abort_flag))) break;
-      const float C = sC[cb * kRows + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&cE[cb]);
+      float C = qmax * ws;  // with wsum: C_b <= max_d Q_d * wsum_b
+      if (wsum == nullptr) {  // without: the scan warps' exact C_b
+        const int cb = static_cast<int>(i % kNC);
+        if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&cF[cb], static_cast<uint32_t>(i / kNC) & 1u, abort_flag))) break;
+        C = sC[cb * kRows + row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cE[cb]);
+      }
       if (row < rows) {
         const bool nan = best != best;
         const int64_t o = static_cast<int64_t>(s) * Nb_max + base + row;
@@ -580,7 +613,7 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
   const bool use_tma = Nb_max % 8 == 0 && make_summary_map(&tmx, kmax, S, CH, Nb_max) == 0 &&
                        make_summary_map(&tmn, kmin, S, CH, Nb_max) == 0;
   const size_t fixed = 2 * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
-                       (2 * kMaxStages + 2 * kNAcc + 4 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
+                       (2 * kMaxStages + 2 * kNAcc + 8 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kHalf));
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + stages * kHalf;
