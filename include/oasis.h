@@ -19,15 +19,20 @@
  *   oasis_sparse_decode_attn  attention of the true query over the slots
  *                             (oasis_sparse_decode_attn_ws: SM-balanced, with a
  *                             caller workspace)
+ * and the tensor-core scoring path that replaces the second and third calls
+ * with the same selections:
+ *   oasis_score_blocks_tc        score estimates with certified error radii
+ *   oasis_select_topk_capped_tc  the exact selection from those estimates
  *
  * Conventions shared by every entry point
  *   Memory.     The caller allocates and owns every buffer.  The library
  *               allocates no memory and keeps no state between calls, except
  *               per process: that each kernel's shared-memory limit was
- *               raised, and for oasis_sparse_decode_attn_noalloc a static
- *               8 MiB device scratch array and its address.  Device pointers
- *               must be device memory or, where stated, host memory the GPU
- *               can address (pinned and mapped).
+ *               raised, the driver's tensor-map encoder entry point, and for
+ *               oasis_sparse_decode_attn_noalloc a static 8 MiB device scratch
+ *               array and its address.  Device pointers must be device memory
+ *               or, where stated, host memory the GPU can address (pinned and
+ *               mapped).
  *   Execution.  Every call enqueues kernels on `stream` (NULL = the legacy
  *               default stream) and returns without synchronising.  Outputs
  *               are valid once the stream reaches that point.
@@ -45,6 +50,34 @@
  *   Blocks.     A logical block holds 16 consecutive tokens; token t of block
  *               b of sequence i is valid when 16*b + t < seq_len[i]
  *               ([XR] §6 default parameters: block size 16).
+ *
+ * Where the interface departs from the plain five-call form (one call per
+ * step, every shape rule checked on the host before a launch), and why:
+ *   - Lengths are per sequence (seq_len[B]) in every call, with B and Hkv in
+ *     place of S = B*Hkv: all KV heads of a sequence share its length, so a
+ *     per-segment copy would only repeat it Hkv times.
+ *   - Rules that depend on the lengths are not host errors: seq_len lives in
+ *     device memory, and checking it on the host would synchronise every call.
+ *     A length beyond the summary capacity (seq_len > 16*Nb_max) or below 0
+ *     sets OASIS_STATUS_SEQ_LEN and is clamped; fewer candidates than K
+ *     (K > nc) is not an error - the rule takes the first min(K, nc).  C > K
+ *     stays a host error.  This is why oasis_build_summary and
+ *     oasis_score_blocks take a status word as well.
+ *   - oasis_stage_blocks takes host_nb, the blocks per segment of the host
+ *     copy, so that a plan entry naming a block outside it is skipped and
+ *     reported (OASIS_STATUS_PLAN_RANGE) instead of read out of bounds.
+ *   - oasis_sparse_decode_attn needs no workspace: the CTAs of a cluster merge
+ *     their partial results in distributed shared memory.  The workspace form
+ *     (ws, ws_bytes, oasis_attn_workspace_bytes) belongs to the SM-balanced
+ *     variant oasis_sparse_decode_attn_ws.
+ *   - oasis_build_summary can also write wsum, and oasis_score_blocks_tc with
+ *     oasis_select_topk_capped_tc are a second scoring path: tensor-core
+ *     estimates with certified radii, from which the selection is exactly the
+ *     one of the fixed-order scores.  oasis_sparse_decode_attn_noalloc and
+ *     oasis_abi_version are conveniences with no counterpart in the pages.
+ *   - No status code is returned for device faults (there is no
+ *     OASIS_EDEVICE): the calls return before the kernels run, so only the
+ *     caller, reading its status word after the stream, can see them.
  *
  * Layouts (element counts; all arrays dense and row-major)
  *   KV tile     [2][16][D] bf16: the block's 16 keys, then its 16 values.
