@@ -46,7 +46,7 @@ WORKLOAD_ID = 5
 def _args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20, help="decode steps timed (one graph replay each)")
+    p.add_argument("--steps", type=int, default=30, help="decode steps timed (one graph replay each)")
     p.add_argument("--warmup", type=int, default=5, help="decode steps run before timing")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=0,
@@ -58,6 +58,8 @@ def _args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-kernels", action="store_true", help="skip the per-kernel timings")
+    p.add_argument("--other-workloads", default="2,3",
+                   help="workload ids also measured (layer-step and kernels, under other_workloads; '' for none)")
     p.add_argument("--bg-streams", type=int, default=3, help="background streams, taken by the layers in turn")
     p.add_argument("--xf-streams", type=int, default=2, help="staging streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
@@ -608,6 +610,15 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = _cpu_baseline(w, args.workload, args.cpu_seconds)
+    others = {}
+    ids = [int(x) for x in args.other_workloads.split(",") if x.strip()] if args.other_workloads else []
+    ids = [i for i in ids if i != args.workload] if world == 1 else []
+    n_drift = len(graphs)
+    if ids:
+        del graphs, wb                      # free the headline state before the other workloads
+        torch.cuda.empty_cache()
+        for i in ids:
+            others[wl.WORKLOADS[i].name] = _other_workload(args, i, dev)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms, "us_per_layer_step": ms * 1e3 / R,
@@ -622,7 +633,7 @@ def run_ours(args):
                     "step": f"one decode step: the whole path (summary update, scoring, capped selection, staging, "
                             f"attention) over each of the {R} layers, layer-pipelined in one CUDA graph; tables "
                             f"advance from step to step, step i uses the queries of drift step i mod "
-                            f"{len(graphs)}",
+                            f"{n_drift}",
                     "l2": f"{R} per-layer buffer sets ({R * per_layer / 1e9:.1f} GB read per step > L2)",
                     "timed_region_s": total_ms / 1e3,
                     "blocks_admitted_last_step": admitted,
@@ -633,6 +644,8 @@ def run_ours(args):
         if kern is not None:
             line["roofline"] = _roofline(w, kern, args.scoring)
             line["kernels_us"] = kern
+        if others:
+            line["other_workloads"] = others
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -659,6 +672,36 @@ def _traffic(kernel, w):
         if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
             return None
     return rec["dram_bytes_per_launch"]
+
+
+def _other_workload(args, wid, dev, steps=10, warmup=3):
+    """Layer-step and per-kernel times of another workload (its own layer count,
+    the same layer-pipelined graph), for the line's other_workloads key."""
+    import torch
+
+    from synth import workload as wl
+    w = wl.WORKLOADS[wid]
+    R = w.layers if w.layers > 1 else 36
+    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring)
+    graphs = wb.graphs(args)
+    wb.reset()
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize(dev)
+    ms = _time_steps(graphs, warmup, steps, dev) / steps
+    st = wb.status()
+    assert st == 0, st
+    kern = _kernel_times(wb, dev)
+    roof = _roofline(w, kern, args.scoring)
+    out = {"workload": _config(w, R)["workload"], "layers": R, "us_per_layer_step": ms * 1e3 / R,
+           "value_gbs": w.headline_bytes_per_layer() / (ms * 1e-3 / R) / 1e9, "steps": steps,
+           "kernels_us": kern,
+           "frac_of_measured_hbm": {"score": w.summary_bytes_per_layer() / (kern["score"] * 1e-6) / 1e9 / roof["peak"],
+                                    "attn": (w.kv_bytes_per_layer() + w.out_bytes_per_layer()) /
+                                    (kern["attn"] * 1e-6) / 1e9 / roof["peak"]}}
+    del graphs, wb
+    torch.cuda.empty_cache()
+    return out
 
 
 def _e2e(args, wb, world, dev, first_step):
