@@ -651,7 +651,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-TRAFFIC_WORKLOAD = "qwen3-8b-layer"  # the workload the committed DRAM-traffic record was captured on
+TRAFFIC_WORKLOAD = "qwen3-235b-attn"  # the workload the committed DRAM-traffic record was captured on
 
 
 def _traffic(kernel, w):
