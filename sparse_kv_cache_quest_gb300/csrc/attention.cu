@@ -411,6 +411,267 @@ __global__ void __launch_bounds__(kThreads)
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
+// ---- 9 to 16 query heads per KV head: the heads split over warp pairs ---------
+// With more than 8 query heads per KV head a warp's chain per tile (S = K.Q^T
+// over 16 heads, their online softmax, O^T += V^T.P^T) is four times that of a
+// 4-head layer, and 4 warps per CTA no longer hide it.  This kernel runs 8
+// warps: warp w takes the slots of partition w % 4 (the slots warp w % 4 of
+// k_attn takes) for the 8 query heads of tile w / 4, so every head's arithmetic
+// and merge order are those of k_attn<KS, 2>.  The two warps of a partition
+// share its slot tiles: the first issues each tile's tensor copy into the pair's
+// ring, both read it, and each releases the stage through an "empty" mbarrier
+// of two arrivals, which the first waits on (bounded) before it copies the next
+// tile into the stage.
+constexpr int kThreadsHS = 256;
+constexpr int kWarpsHS = kThreadsHS / 32;
+constexpr int kPairs = kWarpsHS / 2;  // slot partitions per CTA (as many as k_attn's warps)
+static_assert(kPairs == kWarps, "a pair takes the slots of one k_attn warp");
+
+template <int D>
+struct PlanHS {
+  static constexpr int kNS = 2;                              // ring stages per pair
+  static constexpr int kTile = 64 * D;
+  static constexpr int kRing = kPairs * kNS * kTile;
+  static constexpr int kFull = kRing;                        // kPairs * kNS mbarriers
+  static constexpr int kEmpty = kFull + 8 * kPairs * kNS;    // kPairs * kNS mbarriers
+  static constexpr int kLists = kEmpty + 8 * kPairs * kNS;   // kWarpsHS * kListMax int32
+  static constexpr int kEnd = kLists + 4 * kWarpsHS * kListMax;
+  // combine scratch (floats): each warp's 8 heads (m, l, o), then the CTA's 16
+  static constexpr int kWarpM = 0, kWarpL = kWarpsHS * 8, kWarpO = 2 * kWarpsHS * 8;
+  static constexpr int kCtaM = kWarpO + kWarpsHS * 8 * D, kCtaL = kCtaM + 16, kCtaO = kCtaL + 16;
+  static constexpr int kScratchBytes = 4 * (kCtaO + 16 * D);
+  static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
+};
+
+__device__ __forceinline__ void stage_release(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+template <int KS>
+__global__ void __launch_bounds__(kThreadsHS)
+    k_attn_hs(const __grid_constant__ CUtensorMap tmap, const uint16_t *__restrict__ q,
+              const int32_t *__restrict__ table, int slots, const int32_t *__restrict__ seq_len, int Hkv, int G,
+              float scale_log2, float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
+  constexpr int D = 16 * KS;
+  constexpr int kBoxes = D / 64;
+  using P = PlanHS<D>;
+  constexpr int NS = P::kNS;
+  extern __shared__ unsigned char sm_raw[];
+  const uint32_t raw_addr = smem_addr(sm_raw);
+  unsigned char *sm = sm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(sm);
+  cg::cluster_group cluster = cg::this_cluster();
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pair = warp % kPairs, half = warp / kPairs;  // slot partition, query tile
+  const bool issuer = half == 0;
+  const int g = lane >> 2, t = lane & 3;
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int s = blockIdx.y;
+  const int bseq = s / Hkv, h = s % Hkv;
+  const int Hq = Hkv * G;
+
+  int L = seq_len[bseq];
+  if (L < 0) {
+    if (tid == 0 && rank == 0 && h == 0) report(status, OASIS_STATUS_SEQ_LEN);
+    L = 0;
+  }
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + P::kFull) + pair * NS;
+  uint64_t *empty = reinterpret_cast<uint64_t *>(sm + P::kEmpty) + pair * NS;
+  int32_t *list = reinterpret_cast<int32_t *>(sm + P::kLists) + warp * kListMax;
+  const uint32_t ring = sbase + pair * NS * P::kTile;
+  if (issuer && lane == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 2);  // both warps of the pair
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();  // the pair's barriers exist before its second warp waits on them
+
+  float o[1][KS][4];
+  float m[1][2], l[1][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    m[0][j] = -INFINITY;
+    l[0][j] = 0.0f;
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[0][mt][i] = 0.0f;
+
+  // the partition's non-empty slots, as (slot << 5 | valid tokens); both warps
+  // of a pair build the same list
+  const int nw = CL * kPairs, gw = rank * kPairs + pair;
+  const int nk = slots > gw ? (slots - gw + nw - 1) / nw : 0;
+  const int32_t *trow = table + static_cast<int64_t>(s) * slots;
+  int count = 0;
+  for (int base = 0; base < nk; base += 32) {
+    const int k = base + lane;
+    int nv = 0, slot = 0;
+    if (k < nk) {
+      slot = gw + nw * k;
+      const int blk = trow[slot];
+      const int64_t n = blk < 0 ? 0 : static_cast<int64_t>(L) - static_cast<int64_t>(kBlockTokens) * blk;
+      nv = n <= 0 ? 0 : (n >= kBlockTokens ? kBlockTokens : static_cast<int>(n));
+    }
+    const unsigned mk = __ballot_sync(0xFFFFFFFFu, nv > 0);
+    if (nv > 0) list[count + __popc(mk & ((1u << lane) - 1u))] = (slot << 5) | nv;
+    count += __popc(mk);
+  }
+  __syncwarp();
+  const int row_base = s * slots;
+  auto issue = [&](int c, int stg) {
+    mbar_arrive_expect_tx(&full[stg], P::kTile);
+    const int y = (row_base + (list[c] >> 5)) * 32;
+#pragma unroll
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_load_2d(ring + stg * P::kTile + bx * 4096, &tmap, bx * 64, y, &full[stg]);
+  };
+  if (issuer && lane == 0)
+    for (int c = 0; c < NS && c < count; ++c) issue(c, c);
+
+  // Q^T B-fragments of this warp's 8 query heads (half * 8 + g)
+  uint32_t qb[1][KS][2];
+  {
+    const int qi = half * 8 + g;
+    const uint32_t *row =
+        reinterpret_cast<const uint32_t *>(q + (static_cast<int64_t>(bseq) * Hq + h * G + qi) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qb[0][ks][0] = qi < G ? row[(16 * ks + 2 * t) >> 1] : 0u;
+      qb[0][ks][1] = qi < G ? row[(16 * ks + 8 + 2 * t) >> 1] : 0u;
+    }
+  }
+  int issued = issuer ? min(NS, count) : 0, consumed = 0;
+  bool timed_out = false;
+
+  for (int c = 0; c < count; ++c) {
+    const int stg = c % NS;
+    const bool ok = mbar_wait_bounded(&full[stg], static_cast<uint32_t>(c / NS) & 1u, kWaitTries);
+    if (__any_sync(0xFFFFFFFFu, !ok)) {
+      timed_out = true;
+      break;
+    }
+    attend_tile<KS, 1>(ring + stg * P::kTile, list[c] & 31, qb, scale_log2, o, m, l);
+    __syncwarp();
+    ++consumed;
+    if (lane == 0) stage_release(&empty[stg]);  // this warp is done reading the stage
+    if (issuer && c + NS < count) {
+      // both warps have read the stage: copy the partition's next tile into it
+      int free_ok = 1;
+      if (lane == 0) {
+        free_ok = mbar_wait_bounded(&empty[stg], static_cast<uint32_t>(c / NS) & 1u, kWaitTries);
+        if (free_ok) {
+          fence_proxy_async_smem();
+          issue(c + NS, stg);
+        }
+      }
+      if (!__shfl_sync(0xFFFFFFFFu, free_ok, 0)) {
+        timed_out = true;
+        break;
+      }
+      ++issued;
+    }
+  }
+  if (timed_out) {  // never leave with copies in flight
+    if (lane == 0) report(status, OASIS_STATUS_TIMEOUT);
+    for (int c = consumed; c < issued; ++c)
+      mbar_wait_bounded(&full[c % NS], static_cast<uint32_t>(c / NS) & 1u, kWaitTries);
+  }
+
+  // ---- warp totals: l over the token rows (lanes with equal t); o is complete per thread
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float v = l[0][j];
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+    l[0][j] = v;
+  }
+  __syncthreads();  // every warp is past the rings: the scratch may alias them
+  float *scratch = reinterpret_cast<float *>(sm);
+  float *wm = scratch + P::kWarpM, *wl = scratch + P::kWarpL, *wo = scratch + P::kWarpO;
+  float *cm = scratch + P::kCtaM, *cl = scratch + P::kCtaL, *co = scratch + P::kCtaO;
+  if (g == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      wm[warp * 8 + 2 * t + j] = m[0][j];
+      wl[warp * 8 + 2 * t + j] = l[0][j];
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int qc = 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
+      wo[(warp * 8 + qc) * D + dim] = o[0][mt][i];
+    }
+  __syncthreads();
+  // head qc = 8 * half + j was processed by warps half * kPairs + p, p = 0..kPairs-1
+  // (combined in that order, as k_attn combines its warps)
+  for (int idx = tid; idx < G * D; idx += kThreadsHS) {
+    const int qc = idx / D, d = idx % D;
+    const int w0 = (qc >> 3) * kPairs, j = qc & 7;
+    float M = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) M = fmaxf(M, wm[(w0 + p) * 8 + j]);
+    float acc = 0.0f, ls = 0.0f;
+    if (M > -INFINITY) {
+#pragma unroll
+      for (int p = 0; p < kPairs; ++p) {
+        const float f = exp2f(wm[(w0 + p) * 8 + j] - M);
+        acc += f * wo[((w0 + p) * 8 + j) * D + d];
+        ls += f * wl[(w0 + p) * 8 + j];
+      }
+    }
+    co[qc * D + d] = acc;
+    if (d == 0) {
+      cm[qc] = M;
+      cl[qc] = ls;
+    }
+  }
+  cluster.sync();
+  // cluster merge, as in k_attn
+  {
+    const int n_out = G * D, per = (n_out + CL - 1) / CL;
+    const int e1 = min(n_out, (rank + 1) * per);
+    for (int idx = rank * per + tid; idx < e1; idx += kThreadsHS) {
+      const int qc = idx / D, d = idx % D;
+      float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) {
+        if (r < CL) {
+          mr[r] = cluster.map_shared_rank(cm, r)[qc];
+          lr[r] = cluster.map_shared_rank(cl, r)[qc];
+          orr[r] = cluster.map_shared_rank(co, r)[qc * D + d];
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CL) M = fmaxf(M, mr[r]);
+      float acc = 0.0f, ls = 0.0f;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kMaxCluster; ++r) {
+          if (r < CL) {
+            const float f = exp2f(mr[r] - M);
+            acc += f * orr[r];
+            ls += f * lr[r];
+          }
+        }
+      }
+      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
+      out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
+      if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+    }
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+}
+
 // ---- balanced split with a caller workspace --------------------------------
 // All segments' slots form one flat range of N = S * slots tiles; CTA c of P
 // takes [c*N/P, (c+1)*N/P), so every SM streams the same number of tiles
@@ -684,6 +945,32 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// The pool as a 2-D tensor: rows of D bf16, one 32-row box per 64 dims of a slot.
+cudaError_t make_pool_map(CUtensorMap *tmap, const uint16_t *pool, int D, int S, int slots) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S) * slots * 32};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  return cudaSuccess;
+}
+
+// Cluster size of the split: about two CTAs per SM in all (measured on GB300:
+// larger clusters lose more to co-scheduling than they gain, and deeper
+// per-warp rings or a persistent SM-balanced split with a separate merge kernel
+// were slower), enough that each list of `lists` per CTA fits.
+int cluster_size(int sms, int S, int slots, int lists) {
+  int CL = static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / S)));
+  CL = std::min(CL, slots);
+  while ((slots + CL * lists - 1) / (CL * lists) > kListMax) ++CL;
+  return CL;
+}
+
 template <int KS, int NT>
 cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
                      const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
@@ -691,29 +978,15 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   constexpr int D = 16 * KS;
   using P = Plan<D, 8 * NT>;
   const int S = B * Hkv;
-  // the pool as a 2-D tensor: rows of D bf16, one 32-row box per 64 dims of a slot
-  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-  if (encode == nullptr) return cudaErrorNotSupported;
   CUtensorMap tmap;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S) * slots * 32};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[2] = {64, 32};
-  const cuuint32_t estr[2] = {1, 1};
-  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(pool), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  cudaError_t me = make_pool_map(&tmap, pool, D, S, slots);
+  if (me != cudaSuccess) return me;
   const size_t smem = P::kEnd + 1024;  // + slack for the 1024-byte alignment of the swizzled tiles
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<KS, NT>), kThreads, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
-  // split each segment over a cluster of CL CTAs, about two CTAs per SM in all
-  // (measured on GB300: larger clusters lose more to co-scheduling than they gain,
-  // and deeper per-warp rings or a persistent SM-balanced split with a separate
-  // merge kernel were slower)
-  int CL = static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / S)));
-  CL = std::min(CL, slots);
-  while ((slots + CL * kWarps - 1) / (CL * kWarps) > kListMax) ++CL;  // each warp's list fits
+  // split each segment over a cluster of CL CTAs
+  const int CL = cluster_size(sms, S, slots, kWarps);
   if (CL > kMaxCluster) return cudaErrorInvalidValue;
   LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(kThreads), smem, st);
   cudaLaunchAttribute cl;
@@ -724,6 +997,35 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   lc.add(cl);
   const float scale_log2 = scale * 1.4426950408889634f;
   return cudaLaunchKernelEx(&lc.cfg, k_attn<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
+                            status);
+}
+
+// More than 8 query heads per KV head: the head-split kernel (8 warps per CTA).
+template <int KS>
+cudaError_t launch_hs(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
+                      const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
+                      int32_t *status, cudaStream_t st) {
+  constexpr int D = 16 * KS;
+  using P = PlanHS<D>;
+  const int S = B * Hkv;
+  CUtensorMap tmap;
+  cudaError_t me = make_pool_map(&tmap, pool, D, S, slots);
+  if (me != cudaSuccess) return me;
+  const size_t smem = P::kEnd + 1024;  // + slack for the 1024-byte alignment of the swizzled tiles
+  int sms = 0, per_sm = 0;
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn_hs<KS>), kThreadsHS, smem, &sms, &per_sm);
+  if (e != cudaSuccess) return e;
+  const int CL = cluster_size(sms, S, slots, kPairs);
+  if (CL > kMaxCluster) return cudaErrorInvalidValue;
+  LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(kThreadsHS), smem, st);
+  cudaLaunchAttribute cl;
+  cl.id = cudaLaunchAttributeClusterDimension;
+  cl.val.clusterDim.x = static_cast<unsigned>(CL);
+  cl.val.clusterDim.y = 1;
+  cl.val.clusterDim.z = 1;
+  lc.add(cl);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  return cudaLaunchKernelEx(&lc.cfg, k_attn_hs<KS>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
                             status);
 }
 
@@ -779,10 +1081,10 @@ cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, c
                                       float scale, float *out, float *lse, int32_t *status, cudaStream_t st) {
   if (D == 128) {
     if (G <= 8) return launch_t<8, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
-    return launch_t<8, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+    return launch_hs<8>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
   }
   if (G <= 8) return launch_t<4, 1>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
-  return launch_t<4, 2>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
+  return launch_hs<4>(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, scale, out, lse, status, st);
 }
 
 // Workspace of the balanced split, from one grid size: P pieces' partial
