@@ -514,7 +514,19 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     int nc = 0, seg_cur = -1, used = 0;
     float qmax = 0.0f;  // max_d Q_d of the current segment
     const float gamma = 0x1p-12f, floor_r = 0x1p-110f;
-    for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
+    // this row's wrong-side sum in tile tt (0 past the candidates or without wsum)
+    auto wsum_of = [&](int64_t tt, int ncc) -> float {
+      if (wsum == nullptr || tt >= it.t1) return 0.0f;
+      const int ss = static_cast<int>(tt / tps);
+      const int bb = static_cast<int>(tt - static_cast<int64_t>(ss) * tps) * kRows;
+      return row < ncc - bb ? __ldg(wsum + static_cast<int64_t>(ss) * Nb_max + bb + row) : 0.0f;
+    };
+    int64_t t = it.next(it.t0, &nc);
+    float ws = wsum_of(t, nc);  // loaded a tile ahead: its latency hides behind a whole tile
+    while (t < it.t1) {
+      int nc_next = 0;
+      const int64_t t_next = it.next(t + 1, &nc_next);
+      const float ws_next = wsum_of(t_next, nc_next);
       const int s = static_cast<int>(t / tps);
       const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
       const int rows = min(kRows, nc - base);
@@ -529,10 +541,6 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         ++used;
         seg_cur = s;
       }
-      // this row's wrong-side sum, loaded before the accumulator wait so that the
-      // wait hides its latency
-      const float ws = wsum != nullptr && row < rows ? __ldg(wsum + static_cast<int64_t>(s) * Nb_max + base + row)
-                                                     : 0.0f;
       if (!__all_sync(0xFFFFFFFFu, wait_or_abort(&accF[acc], static_cast<uint32_t>(i / kNAcc) & 1u, abort_flag)))
         break;  // the whole warp leaves together
       tc_fence_after();
@@ -567,6 +575,9 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         radius[o] = nan ? __uint_as_float(0x7F800000u) : fmaf(gamma, fabsf(best) + 2.0f * C, floor_r);
       }
       ++i;
+      t = t_next;
+      nc = nc_next;
+      ws = ws_next;
     }
   }
 
