@@ -144,40 +144,52 @@ __device__ __forceinline__ uint32_t neg_halves(uint32_t x) {
   return r;
 }
 
+// The CTA's tiles [t0, t1) in segment-major order (tile j of segment s =
+// blocks j*kRows .. of s, global index t = s*tps + j); a tile is work when its
+// first block is a candidate of its segment.  begin() divides once; advance()
+// steps without dividing and reads a segment's length when it enters it.
 struct TileIter {
-  // the CTA's tiles [t0, t1) in segment-major order; a tile is work when its
-  // first block is a candidate of its segment
   int64_t t0, t1;
   int tps, Hkv, W, Nb_max;
   const int32_t *seq_len;
-  int s_last = -1, nc_last = 0;  // the last segment asked about (a load per segment, not per tile)
-  __device__ int nc_of(int s) {
-    if (s != s_last) {
-      int L = __ldg(seq_len + s / Hkv);
-      L = L < 0 ? 0 : (L > Nb_max * kBlockTokens ? Nb_max * kBlockTokens : L);
-      s_last = s;
-      nc_last = ceil_div(L, kBlockTokens) - W;
-    }
-    return nc_last;
+  int s = 0, j = 0, nc = 0;  // the current work tile: segment, tile in it, candidates of the segment
+  int64_t t = 0;
+  __device__ int nc_of(int seg) const {
+    int L = __ldg(seq_len + seg / Hkv);
+    L = L < 0 ? 0 : (L > Nb_max * kBlockTokens ? Nb_max * kBlockTokens : L);
+    return ceil_div(L, kBlockTokens) - W;
   }
-  // first work tile at or after t (t1 if none); nc of its segment in *nc
-  __device__ int64_t next(int64_t t, int *nc) {
+  // the first work tile at or after the current position (t = t1 if none)
+  __device__ void settle() {
     while (t < t1) {
-      const int s = static_cast<int>(t / tps);
-      const int n = nc_of(s);
-      const int64_t seg_end = std::min<int64_t>(t1, static_cast<int64_t>(s + 1) * tps);
-      if (static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows < n) {
-        *nc = n;
-        return t;
+      if (j < tps && j * kRows < nc) return;
+      ++s;
+      j = 0;
+      t = static_cast<int64_t>(s) * tps;
+      if (t >= t1) {
+        t = t1;
+        return;
       }
-      t = seg_end;  // the remaining tiles of this segment are past its candidates
+      nc = nc_of(s);
     }
-    return t1;
   }
-  // does segment s have a work tile in [t0, t1)?
-  __device__ bool active(int s) {
-    const int64_t first = std::max<int64_t>(t0, static_cast<int64_t>(s) * tps);
-    return static_cast<int>(first - static_cast<int64_t>(s) * tps) * kRows < nc_of(s);
+  __device__ void begin() {
+    s = static_cast<int>(t0 / tps);
+    j = static_cast<int>(t0 - static_cast<int64_t>(s) * tps);
+    t = t0;
+    nc = t0 < t1 ? nc_of(s) : 0;
+    settle();
+  }
+  __device__ bool valid() const { return t < t1; }
+  __device__ void advance() {
+    ++j;
+    ++t;
+    settle();
+  }
+  // does segment seg have a work tile in [t0, t1)?
+  __device__ bool active(int seg) const {
+    const int64_t first = std::max<int64_t>(t0, static_cast<int64_t>(seg) * tps);
+    return static_cast<int>(first - static_cast<int64_t>(seg) * tps) * kRows < nc_of(seg);
   }
 };
 
@@ -265,18 +277,17 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   if (warp == 0) {
     // ---------------- producer: one copy per half-tile into the stage ring
     if (lane == 0) {
-      int64_t issued = 0;  // half-tiles
-      int nc = 0;
+      int64_t issued = 0;    // half-tiles
+      int st = 0;            // issued % stages
+      uint32_t round = 0;    // issued / stages
       bool ok = true;
-      for (int64_t t = it.next(it.t0, &nc); t < it.t1 && ok; t = it.next(t + 1, &nc)) {
-        const int s = static_cast<int>(t / tps);
-        const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
-        const int rows = min(kRows, nc - base);
+      for (it.begin(); it.valid() && ok; it.advance()) {
+        const int s = it.s;
+        const int base = it.j * kRows;
+        const int rows = min(kRows, it.nc - base);
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
-          const int st = static_cast<int>(issued % stages);
-          if (issued >= stages &&
-              !wait_or_abort(&empty[st], static_cast<uint32_t>((issued / stages) - 1) & 1u, abort_flag)) {
+          if (issued >= stages && !wait_or_abort(&empty[st], (round - 1u) & 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -296,6 +307,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               bulk_g2s(dst + c * kChunkBytes, g + static_cast<int64_t>(c) * Nb_max, bytes, &full[st]);
           }
           ++issued;
+          if (++st == stages) {
+            st = 0;
+            ++round;
+          }
         }
       }
       // never leave with copies in flight: wait for the last stages issued
@@ -307,11 +322,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<N>();
       int64_t i = 0, u = 0;  // tiles, half-tiles
+      int st = 0;            // u % stages
+      uint32_t round = 0;    // u / stages
       int seg_prev = -1, nseg = 0, buf = 0;
-      int nc = 0;
       bool ok = true;
-      for (int64_t t = it.next(it.t0, &nc); t < it.t1 && ok; t = it.next(t + 1, &nc)) {
-        const int s = static_cast<int>(t / tps);
+      for (it.begin(); it.valid() && ok; it.advance()) {
+        const int s = it.s;
         if (s != seg_prev) {  // the query operand of this segment
           if (seg_prev >= 0) tc_commit(&bqE[buf]);  // the previous segment's operand is free once its MMAs are done
           buf = nseg & 1;
@@ -327,8 +343,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const uint32_t b0 = smem_addr(sB + static_cast<size_t>(buf) * kBBytes);
 #pragma unroll 1
         for (int h = 0; h < 2 && ok; ++h) {
-          const int st = static_cast<int>(u % stages);
-          ok = wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u, abort_flag);
+          ok = wait_or_abort(&full[st], round & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t a0 = smem_addr(sA + static_cast<size_t>(st) * kHalf);
@@ -341,6 +356,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
           }
           tc_commit(&empty[st]);  // the half-stage is free once these MMAs have read it
           ++u;
+          if (++st == stages) {
+            st = 0;
+            ++round;
+          }
         }
         if (!ok) break;
         tc_commit(&accF[acc]);
@@ -442,28 +461,27 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       // waits until its buffer's previous segment is done with it)
       while (next_build <= s_last) build_next();
     } else {
-      int64_t i = 0, u = 0;  // tiles, half-tiles
+      int64_t i = 0;         // tiles
+      int st = 0;            // half-tiles % stages
+      uint32_t round = 0;    // half-tiles / stages
       int seg_prev = -1, used = 0, bq = 0;
-      int nc = 0;
-      for (int64_t t = it.next(it.t0, &nc); t < it.t1; t = it.next(t + 1, &nc)) {
-        const int s = static_cast<int>(t / tps);
+      for (it.begin(); it.valid(); it.advance()) {
+        const int s = it.s;
         if (s != seg_prev) {
           if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is rebuilt for the next-but-one
           bq = used & 1;
           ++used;
           seg_prev = s;
         }
-        const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
-        const int rows = min(kRows, nc - base);
+        const int base = it.j * kRows;
+        const int rows = min(kRows, it.nc - base);
         // C_b: the summary values on the wrong side of zero, weighted by Q_d (kmax
         // half: |kmax| where kmax < 0; kmin half: kmin where kmin > 0), from the stages
         float C = 0.0f;
         {
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
-            const int st = static_cast<int>(u % stages);
-            const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], static_cast<uint32_t>(u / stages) & 1u,
-                                                                   abort_flag));
+            const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], round & 1u, abort_flag));
             if (got && row < rows) {
               const uint8_t *A = sA + static_cast<size_t>(st) * kHalf + row * 16;
               // fast test: any sign bit set among the kmax half (h = 0) / any clear among
@@ -493,7 +511,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
             }
             __syncwarp();
             if (got && lane == 0) mbar_arrive(&empty[st]);
-            ++u;
+            if (++st == stages) {
+              st = 0;
+              ++round;
+            }
           }
         }
         const int cb = static_cast<int>(i % kNC);
@@ -511,25 +532,25 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     const int quad = warp & 3;                 // the TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     int64_t i = 0;
-    int nc = 0, seg_cur = -1, used = 0;
+    int seg_cur = -1, used = 0;
     float qmax = 0.0f;  // max_d Q_d of the current segment
     const float gamma = 0x1p-12f, floor_r = 0x1p-110f;
     // this row's wrong-side sum in tile tt (0 past the candidates or without wsum)
-    auto wsum_of = [&](int64_t tt, int ncc) -> float {
-      if (wsum == nullptr || tt >= it.t1) return 0.0f;
-      const int ss = static_cast<int>(tt / tps);
-      const int bb = static_cast<int>(tt - static_cast<int64_t>(ss) * tps) * kRows;
-      return row < ncc - bb ? __ldg(wsum + static_cast<int64_t>(ss) * Nb_max + bb + row) : 0.0f;
+    auto wsum_of = [&](const TileIter &w) -> float {
+      if (wsum == nullptr || !w.valid()) return 0.0f;
+      const int bb = w.j * kRows;
+      return row < w.nc - bb ? __ldg(wsum + static_cast<int64_t>(w.s) * Nb_max + bb + row) : 0.0f;
     };
-    int64_t t = it.next(it.t0, &nc);
-    float ws = wsum_of(t, nc);  // loaded a tile ahead: its latency hides behind a whole tile
-    while (t < it.t1) {
-      int nc_next = 0;
-      const int64_t t_next = it.next(t + 1, &nc_next);
-      const float ws_next = wsum_of(t_next, nc_next);
-      const int s = static_cast<int>(t / tps);
-      const int base = static_cast<int>(t - static_cast<int64_t>(s) * tps) * kRows;
-      const int rows = min(kRows, nc - base);
+    TileIter cur = it;
+    cur.begin();
+    float ws = wsum_of(cur);  // loaded a tile ahead: its latency hides behind a whole tile
+    while (cur.valid()) {
+      TileIter nxt = cur;
+      nxt.advance();
+      const float ws_next = wsum_of(nxt);
+      const int s = cur.s;
+      const int base = cur.j * kRows;
+      const int rows = min(kRows, cur.nc - base);
       const int acc = static_cast<int>(i % kNAcc);
       if (s != seg_cur) {  // take the segment's max_d Q_d and free its slot
         const int b = used & 1;
@@ -575,8 +596,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         radius[o] = nan ? __uint_as_float(0x7F800000u) : fmaf(gamma, fabsf(best) + 2.0f * C, floor_r);
       }
       ++i;
-      t = t_next;
-      nc = nc_next;
+      cur = nxt;
       ws = ws_next;
     }
   }
