@@ -313,8 +313,10 @@ def test_stage_copies_exactly_the_plan():
 # ------------------------------------------------------------------ attention
 
 @pytest.mark.parametrize("ws", [False, True])
+# G > 8 runs the head-split kernel: (64, 12) its d_h 64 form, (128, 9) a second half
+# with one head, (128, 16, 3) slot partitions left empty
 @pytest.mark.parametrize("D,G,slots", [(128, 4, 128), (64, 2, 37), (128, 1, 5), (128, 8, 64), (128, 16, 128),
-                                       (64, 5, 20), (128, 3, 1)])
+                                       (64, 5, 20), (128, 3, 1), (64, 12, 40), (128, 9, 33), (128, 16, 3)])
 def test_attention_within_tolerance(D, G, slots, ws):
     rng = np.random.default_rng(D + G * 13 + slots)
     B, Hkv, Nb = 2, 3, 300
