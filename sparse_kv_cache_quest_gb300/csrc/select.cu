@@ -29,7 +29,7 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr size_t kStaticSmemBound = 4096;  // >= the kernel's static shared memory (3 KiB of histograms + scalars)
 
@@ -227,21 +227,20 @@ __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, 
 // the fixed-order arithmetic, and the selection then runs on the mixed scores:
 // the settled members keep their side, the recomputed ones are ordered
 // exactly, so every set equals the one the exact scores give.
-constexpr int kBatch = 32;  // blocks recomputed per pass
+constexpr int kBatch = 8;  // blocks recomputed per pass
 
 // Byte offsets of the certified kernel's extra shared memory, from the start
 // of the dynamic allocation; one definition serves the kernel's pointers and
 // the launcher's allocation size.
 struct CertLayout {
-  size_t stage, qsm, res, bmX, xl, rankE, rad, end;
+  size_t stage, res, bmX, xl, rankE, rad, end;
 };
 __host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max, int K, int CH, int Nq) {
   const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
   const size_t Nq4 = (static_cast<size_t>(Nq) + 3) & ~static_cast<size_t>(3);
   CertLayout L;
   L.stage = (base_bytes + 15) & ~static_cast<size_t>(15);
-  L.qsm = L.stage + 16 * static_cast<size_t>(kBatch) * (2 * CH + 1);      // uint4 [kBatch][2*CH + 1]
-  L.res = L.qsm + 4 * static_cast<size_t>(CH) * 8 * Nq4;                 // float [D][Nq4]
+  L.res = L.stage + 16 * static_cast<size_t>(kBatch) * (2 * CH + 1);      // uint4 [kBatch][2*CH + 1]
   L.bmX = L.res + 4 * static_cast<size_t>(kBatch) * Nq4;                 // float [kBatch][Nq4]
   L.xl = L.bmX + 4 * words;                                              // uint32 [words]
   L.rankE = L.xl + 4 * static_cast<size_t>(Nb_max);                      // int32 [Nb_max]
@@ -293,13 +292,16 @@ __device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps
 // kmax_d : kmin_d), one rounding per term; max over the queries, NaN kept).
 // Writes them to srow and their keys to keys, zeroes their radii in rad (a
 // recomputed score is exact), marks them in bmX.  A thread takes one (block,
-// query) pair at a time; qsm holds the queries as [d][Nq4].  The max over a
-// block's queries is taken by one warp as the largest order key of the sums
-// (+0 above -0), which does not depend on the order of the reduction.
+// query) pair at a time and reads the query from global memory (query j =
+// draft j / G of head j % G: row qseg + ((j / G) * Hq + j % G) * D; a handful of
+// blocks per segment are recomputed, so the reads stay in cache and the CTA
+// keeps no copy of the queries).  The max over a block's queries is taken by
+// one warp as the largest order key of the sums (+0 above -0), which does not
+// depend on the order of the reduction.
 template <int CH>
 __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
-                                 int Nq, const float *qsm, uint4 *stage, float *res, float *srow, uint32_t *keys,
-                                 float *rad, uint32_t *bmX, SelScalars &sc) {
+                                 int Nq, const uint16_t *qseg, int G, int Hq, uint4 *stage, float *res, float *srow,
+                                 uint32_t *keys, float *rad, uint32_t *bmX, SelScalars &sc) {
   constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Nq4 = (Nq + 3) & ~3;
@@ -313,18 +315,20 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
     __syncthreads();
     for (int i = tid; i < nb * Nq; i += kThreads) {
       const int e = i / Nq, j = i - e * Nq;
+      const int jd = j / G;
       const uint4 *st = stage + e * ES;
-      const float *qj = qsm + j;
+      const uint4 *qj = reinterpret_cast<const uint4 *>(qseg + (static_cast<int64_t>(jd) * Hq + (j - jd * G)) * (8 * CH));
       float acc = 0.0f;
 #pragma unroll 2
       for (int c = 0; c < CH; ++c) {
-        const uint4 mn = st[c], mx = st[CH + c];
+        const uint4 mn = st[c], mx = st[CH + c], qv = __ldg(qj + c);
         const uint32_t wn[4] = {mn.x, mn.y, mn.z, mn.w}, wx[4] = {mx.x, mx.y, mx.z, mx.w};
+        const uint32_t wq[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const float kn = (t & 1) ? bf16_hi(wn[t >> 1]) : bf16_lo(wn[t >> 1]);
           const float kx = (t & 1) ? bf16_hi(wx[t >> 1]) : bf16_lo(wx[t >> 1]);
-          const float q = qj[(c * 8 + t) * Nq4];
+          const float q = (t & 1) ? bf16_hi(wq[t >> 1]) : bf16_lo(wq[t >> 1]);
           acc = fmaf(q, q >= 0.0f ? kx : kn, acc);  // exact product, one rounding
         }
       }
@@ -401,13 +405,16 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   const int Nq = CERTIFY ? ca.G * ca.Nd : 0;
   const CertLayout cl = cert_layout(reinterpret_cast<unsigned char *>(fSorted + cap) - smraw, Nb_max, K, CH, Nq);
   uint4 *stage = reinterpret_cast<uint4 *>(smraw + cl.stage);      // staged summaries of recomputed blocks
-  float *qsm = reinterpret_cast<float *>(smraw + cl.qsm);          // [D][Nq4] queries
   float *res = reinterpret_cast<float *>(smraw + cl.res);          // [kBatch][Nq4] per-query sums
   uint32_t *bmX = reinterpret_cast<uint32_t *>(smraw + cl.bmX);    // [words] recomputed blocks
   int32_t *xl = reinterpret_cast<int32_t *>(smraw + cl.xl);        // [Nb_max] blocks to recompute
   int32_t *rankE = reinterpret_cast<int32_t *>(smraw + cl.rankE);  // [K]
   float *rad = reinterpret_cast<float *>(smraw + cl.rad);          // [Nb_max] radii, 0 once recomputed
   float *srow_w = CERTIFY ? ca.scores + static_cast<int64_t>(s) * Nb_max : nullptr;
+  // the segment's draft queries: [Nd][Hq][D] rows of sequence s / Hkv from head (s % Hkv) * G on
+  const int Hq_c = CERTIFY ? Hkv * ca.G : 0;
+  const uint16_t *qseg = CERTIFY ? ca.qdraft + (static_cast<int64_t>(s / Hkv) * ca.Nd * Hq_c + (s % Hkv) * ca.G) * D
+                                 : nullptr;
   const float *rrow = CERTIFY ? ca.radius + static_cast<int64_t>(s) * Nb_max : nullptr;
   const uint4 *gmin = CERTIFY ? reinterpret_cast<const uint4 *>(ca.kmin) + static_cast<int64_t>(s) * CH * Nb_max
                               : nullptr;
@@ -428,21 +435,8 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
     sc.nN = sc.nE = sc.nF = sc.nEmpty = 0;
   }
   for (int i = tid; i < 256; i += kThreads) hist[0][i] = 0u;
-  if constexpr (CERTIFY) {
+  if constexpr (CERTIFY)
     for (int i = tid; i < words; i += kThreads) bmX[i] = 0u;
-    // the segment's query vectors, widened: qsm[d][j], j = draft * G + head in group,
-    // padded to a multiple of 4 by repeating the last one
-    const int Hq = Hkv * ca.G, bseq = s / Hkv, h = s % Hkv, Nq4 = (Nq + 3) & ~3;
-    // (consecutive threads take consecutive queries: the stores are free of bank conflicts)
-    for (int i = tid; i < Nq4 * CH; i += kThreads) {
-      const int j = i % Nq4, c = i / Nq4, jq = min(j, Nq - 1), jd = jq / ca.G, g = jq % ca.G;
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-          ca.qdraft + ((static_cast<int64_t>(bseq) * ca.Nd + jd) * Hq + h * ca.G + g) * D + c * 8));
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-      for (int t = 0; t < 8; ++t) qsm[(c * 8 + t) * Nq4 + j] = (t & 1) ? bf16_hi(w4[t >> 1]) : bf16_lo(w4[t >> 1]);
-    }
-  }
   bool nan = false;
   const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
   for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
@@ -499,7 +493,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
         if (!(lo > hi_out[0]) && !(hi < lo_in[0])) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, rad, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, rad, bmX, sc);
       // T = the settled members of the estimated T, and as many of the recomputed
       // ones as the estimated T held, best first by the exact keys
       int need = 0;
@@ -616,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
         if (!bit(bmX, b) && !(lo > e_hi) && !(hi < e_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qsm, stage, res, srow_w, keys, rad, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, rad, bmX, sc);
       for (int i = tid; i < nN; i += kThreads) {
         const int b = composite_block(listN[i]);
         listN[i] = composite(keys[b], b);
