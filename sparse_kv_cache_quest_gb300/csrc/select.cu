@@ -227,13 +227,13 @@ __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, 
 // the fixed-order arithmetic, and the selection then runs on the mixed scores:
 // the settled members keep their side, the recomputed ones are ordered
 // exactly, so every set equals the one the exact scores give.
-constexpr int kBatch = 8;  // blocks recomputed per pass
+constexpr int kBatch = 4;  // blocks recomputed per pass
 
 // Byte offsets of the certified kernel's extra shared memory, from the start
 // of the dynamic allocation; one definition serves the kernel's pointers and
 // the launcher's allocation size.
 struct CertLayout {
-  size_t stage, res, bmX, xl, rankE, rad, end;
+  size_t stage, res, bmX, xl, rankE, end;
 };
 __host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max, int K, int CH, int Nq) {
   const size_t words = (static_cast<size_t>(Nb_max) + 31) / 32;
@@ -244,8 +244,7 @@ __host__ __device__ inline CertLayout cert_layout(size_t base_bytes, int Nb_max,
   L.bmX = L.res + 4 * static_cast<size_t>(kBatch) * Nq4;                 // float [kBatch][Nq4]
   L.xl = L.bmX + 4 * words;                                              // uint32 [words]
   L.rankE = L.xl + 4 * static_cast<size_t>(Nb_max);                      // int32 [Nb_max]
-  L.rad = L.rankE + 4 * static_cast<size_t>(K);                          // int32 [K]
-  L.end = L.rad + 4 * static_cast<size_t>(Nb_max);                       // float [Nb_max]
+  L.end = L.rankE + 4 * static_cast<size_t>(K);                          // int32 [K]
   return L;
 }
 
@@ -290,8 +289,8 @@ __device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps
 // Fixed-order fp32 scores of the listed blocks (the oasis_score_blocks
 // arithmetic: per query, sum over d ascending from +0 of q_d * (q_d >= 0 ?
 // kmax_d : kmin_d), one rounding per term; max over the queries, NaN kept).
-// Writes them to srow and their keys to keys, zeroes their radii in rad (a
-// recomputed score is exact), marks them in bmX.  A thread takes one (block,
+// Writes them to srow and their keys to keys and marks them in bmX (a
+// recomputed score is exact: its radius counts as 0).  A thread takes one (block,
 // query) pair at a time and reads the query from global memory (query j =
 // draft j / G of head j % G: row qseg + ((j / G) * Hq + j % G) * D; a handful of
 // blocks per segment are recomputed, so the reads stay in cache and the CTA
@@ -301,7 +300,7 @@ __device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps
 template <int CH>
 __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
                                  int Nq, const uint16_t *qseg, int G, int Hq, uint4 *stage, float *res, float *srow,
-                                 uint32_t *keys, float *rad, uint32_t *bmX, SelScalars &sc) {
+                                 uint32_t *keys, uint32_t *bmX, SelScalars &sc) {
   constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Nq4 = (Nq + 3) & ~3;
@@ -352,7 +351,6 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
         srow[b] = v;
         bool isn = false;
         keys[b] = score_key(v, isn);
-        rad[b] = 0.0f;
         if (isn) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
         atomicOr(&bmX[b >> 5], 1u << (b & 31));
       }
@@ -362,9 +360,10 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
 }
 
 // interval of block b from its key and radius (a recomputed block has radius 0)
-__device__ __forceinline__ void interval(const uint32_t *keys, const float *rad, int b, float &lo, float &hi) {
+__device__ __forceinline__ void interval(const uint32_t *keys, const float *rrow, const uint32_t *bmX, int b,
+                                         float &lo, float &hi) {
   const float v = key_score(keys[b]);
-  const float r = rad[b];
+  const float r = bit(bmX, b) ? 0.0f : __ldg(rrow + b);
   lo = v - r;
   hi = v + r;
 }
@@ -409,7 +408,6 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   uint32_t *bmX = reinterpret_cast<uint32_t *>(smraw + cl.bmX);    // [words] recomputed blocks
   int32_t *xl = reinterpret_cast<int32_t *>(smraw + cl.xl);        // [Nb_max] blocks to recompute
   int32_t *rankE = reinterpret_cast<int32_t *>(smraw + cl.rankE);  // [K]
-  float *rad = reinterpret_cast<float *>(smraw + cl.rad);          // [Nb_max] radii, 0 once recomputed
   float *srow_w = CERTIFY ? ca.scores + static_cast<int64_t>(s) * Nb_max : nullptr;
   // the segment's draft queries: [Nd][Hq][D] rows of sequence s / Hkv from head (s % Hkv) * G on
   const int Hq_c = CERTIFY ? Hkv * ca.G : 0;
@@ -440,8 +438,6 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   bool nan = false;
   const float *srow = scores + static_cast<int64_t>(s) * Nb_max;
   for (int b = tid; b < nc; b += kThreads) keys[b] = score_key(srow[b], nan);
-  if constexpr (CERTIFY)
-    for (int b = tid; b < nc; b += kThreads) rad[b] = rrow[b];
   __syncthreads();
   if (nan) atomicOr(&sc.err, OASIS_STATUS_NAN_SCORE);
 
@@ -478,7 +474,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       float lo_in[1] = {INFINITY}, hi_out[1] = {-INFINITY};
       for (int b = tid; b < nc; b += kThreads) {
         float lo, hi;
-        interval(keys, rad, b, lo, hi);
+        interval(keys, rrow, bmX, b, lo, hi);
         if (lo != lo || hi != hi) continue;  // NaN estimate: recomputed below
         if (bit(bmT, b))
           lo_in[0] = fminf(lo_in[0], lo);
@@ -489,11 +485,11 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       block_minmax<1>(lo_in, hi_out, red);
       for (int b = tid; b < nc; b += kThreads) {
         float lo, hi;
-        interval(keys, rad, b, lo, hi);
+        interval(keys, rrow, bmX, b, lo, hi);
         if (!(lo > hi_out[0]) && !(hi < lo_in[0])) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, rad, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
       // T = the settled members of the estimated T, and as many of the recomputed
       // ones as the estimated T held, best first by the exact keys
       int need = 0;
@@ -580,7 +576,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       float lo_[2] = {INFINITY, INFINITY}, hi_[2] = {-INFINITY, -INFINITY};
       for (int i = tid; i < nN; i += kThreads) {
         float lo, hi;
-        interval(keys, rad, composite_block(listN[i]), lo, hi);
+        interval(keys, rrow, bmX, composite_block(listN[i]), lo, hi);
         if (rankN[i] < nA)
           lo_[0] = fminf(lo_[0], lo);
         else
@@ -588,7 +584,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       }
       for (int i = tid; i < nE; i += kThreads) {
         float lo, hi;
-        interval(keys, rad, composite_block(listE[i]), lo, hi);
+        interval(keys, rrow, bmX, composite_block(listE[i]), lo, hi);
         if (rankE[i] < nEvict)
           hi_[1] = fmaxf(hi_[1], hi);  // evicted by the estimates
         else
@@ -600,17 +596,17 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       for (int i = tid; i < nN && certA; i += kThreads) {
         const int b = composite_block(listN[i]);
         float lo, hi;
-        interval(keys, rad, b, lo, hi);
+        interval(keys, rrow, bmX, b, lo, hi);
         if (!bit(bmX, b) && !(lo > a_hi) && !(hi < a_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       for (int i = tid; i < nE && certE; i += kThreads) {
         const int b = composite_block(listE[i]);
         float lo, hi;
-        interval(keys, rad, b, lo, hi);
+        interval(keys, rrow, bmX, b, lo, hi);
         if (!bit(bmX, b) && !(lo > e_hi) && !(hi < e_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, rad, bmX, sc);
+      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
       for (int i = tid; i < nN; i += kThreads) {
         const int b = composite_block(listN[i]);
         listN[i] = composite(keys[b], b);
