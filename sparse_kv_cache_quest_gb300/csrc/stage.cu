@@ -7,12 +7,13 @@
 // The host copy of the full cache is pinned, mapped host memory that the GPU
 // reads directly (zero-copy): on a Grace-Blackwell node the loads travel over
 // NVLink-C2C, elsewhere over PCIe.  The copy is bound by that link, not by the
-// SMs, so the kernel is kept small: kCtas CTAs whose warps walk the plan
-// entries (segment-major) with a stride, one tile per warp at a time in two
-// halves, all of a half's 16-byte loads issued before its stores.  That keeps
-// about a megabyte in flight, several times what the link needs to stay busy,
-// at 48 registers a thread, so a staging CTA fits on an SM beside the CTAs of
-// the scoring or attention kernels that run on other streams.
+// SMs, so the kernel is kept small: kCtas CTAs of 4 warps that walk the plan
+// entries (segment-major) with a stride, one tile per warp at a time, all of
+// the tile's 16-byte loads issued before its stores.  That keeps about a
+// megabyte in flight, several times what the link needs to stay busy, in CTAs
+// of about 10k registers, so a staging CTA fits on an SM beside the CTAs of the
+// scoring or attention kernels that run on other streams.
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -20,12 +21,12 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCtas = 32;
-constexpr int kMaxPerLane = 8;   // 16-byte loads per lane for half a tile at D = 128
+constexpr int kMaxPerLane = 16;  // 16-byte loads per lane for one tile at D = 128
 
-__global__ void __launch_bounds__(kThreads, 5) k_stage(const unsigned char *__restrict__ host, int64_t seg_stride,
+__global__ void __launch_bounds__(kThreads) k_stage(const unsigned char *__restrict__ host, int64_t seg_stride,
                                                     int host_nb, const oasis_xfer_t *__restrict__ plan,
                                                     const int32_t *__restrict__ plan_count, int cap, int S, int D,
                                                     uint16_t *__restrict__ pool, int slots, int32_t *status) {
@@ -48,17 +49,13 @@ __global__ void __launch_bounds__(kThreads, 5) k_stage(const unsigned char *__re
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(host + s * seg_stride + x.src_block * (64LL * D));
     uint4 *dst = reinterpret_cast<uint4 *>(pool + (static_cast<int64_t>(s) * slots + x.dst_slot) * 32 * D);
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      const int o = half * kMaxPerLane * 32;
-      uint4 v[kMaxPerLane];
+    uint4 v[kMaxPerLane];
 #pragma unroll
-      for (int u = 0; u < kMaxPerLane; ++u)
-        if (o + u * 32 + lane < n16) v[u] = src[o + u * 32 + lane];
+    for (int u = 0; u < kMaxPerLane; ++u)
+      if (u * 32 + lane < n16) v[u] = src[u * 32 + lane];
 #pragma unroll
-      for (int u = 0; u < kMaxPerLane; ++u)
-        if (o + u * 32 + lane < n16) dst[o + u * 32 + lane] = v[u];
-    }
+    for (int u = 0; u < kMaxPerLane; ++u)
+      if (u * 32 + lane < n16) dst[u * 32 + lane] = v[u];
   }
 }
 
