@@ -29,8 +29,7 @@
 namespace oasis {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxWarps = 16;  // 512 threads at most (the thread count NT is a template parameter)
 constexpr size_t kStaticSmemBound = 4096;  // >= the kernel's static shared memory (3 KiB of histograms + scalars)
 
 __device__ __forceinline__ uint32_t score_key(float f, bool &nan) {
@@ -57,8 +56,10 @@ __device__ __forceinline__ int composite_block(uint64_t c) {
 
 __device__ __forceinline__ bool bit(const uint32_t *bm, int b) { return (bm[b >> 5] >> (b & 31)) & 1u; }
 
-// Exclusive prefix sum of v over the CTA (all threads call it).
+// Exclusive prefix sum of v over the CTA of NT threads (all threads call it).
+template <int NT>
 __device__ int block_exclusive_scan(int v, int *warp_tot) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -89,14 +90,16 @@ struct SelScalars {
   int nN, nE, nF, nEmpty;
   uint32_t digit, dcount;  // radix select: the pass's digit and the keys in its bin
   int remaining;
-  int warp_tot[kWarps];
+  int warp_tot[kMaxWarps];
 };
 
-static_assert(sizeof(SelScalars) + 2 * 256 * sizeof(uint32_t) + 4 * kWarps * sizeof(float) + 64 <= kStaticSmemBound,
+static_assert(sizeof(SelScalars) + 2 * 256 * sizeof(uint32_t) + 4 * kMaxWarps * sizeof(float) + 64 <= kStaticSmemBound,
               "static shared memory bound");
 
-// Sum of v over the CTA (all threads call it, all get the sum).
+// Sum of v over the CTA of NT threads (all threads call it, all get the sum).
+template <int NT>
 __device__ int block_sum(int v, int *warp_tot) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -122,9 +125,10 @@ __device__ int block_sum(int v, int *warp_tot) {
 // in the last place of each other), which the certified selection accepts (it
 // settles any K candidates).  bmT must be clear and hist[0] zero; all threads
 // call it; the caller synchronises before reading bmT.
-template <int PASSES>
+template <int PASSES, int NT>
 __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, uint32_t (*hist)[256],
                             SelScalars &sc) {
+  constexpr int kThreads = NT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (nc <= K) {
     for (int b0 = warp * 32; b0 < nc; b0 += kThreads) {
@@ -201,7 +205,7 @@ __device__ void topk_bitmap(const uint32_t *keys, int nc, int K, uint32_t *bmT, 
   const int lo = min(nc, tid * per), hi = min(nc, lo + per);
   int ties = 0;
   for (int b = lo; b < hi; ++b) ties += (keys[b] & pmask) == prefix;
-  int before = block_exclusive_scan(ties, sc.warp_tot);
+  int before = block_exclusive_scan<NT>(ties, sc.warp_tot);
   for (int b = lo; b < hi; ++b) {
     const uint32_t km = keys[b] & pmask;
     bool in = km > prefix;
@@ -257,8 +261,9 @@ struct CertArgs {
 
 // CTA-wide min of each lo[k] and max of each hi[k] (NaN ignored), one
 // barrier pair for all of them; every thread gets the results.
-template <int N>
-__device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps]) {
+template <int N, int NT>
+__device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kMaxWarps]) {
+  constexpr int kWarps = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int k = 0; k < N; ++k) {
@@ -297,11 +302,12 @@ __device__ void block_minmax(float (&lo)[N], float (&hi)[N], float (*red)[kWarps
 // keeps no copy of the queries).  The max over a block's queries is taken by
 // one warp as the largest order key of the sums (+0 above -0), which does not
 // depend on the order of the reduction.
-template <int CH>
+template <int CH, int NT>
 __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, const uint4 *gmax, int Nb_max,
                                  int Nq, const uint16_t *qseg, int G, int Hq, uint4 *stage, float *res, float *srow,
                                  uint32_t *keys, uint32_t *bmX, SelScalars &sc) {
   constexpr int ES = 2 * CH + 1;  // staged entry: kmin chunks, kmax chunks, one pad (bank spread)
+  constexpr int kThreads = NT, kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Nq4 = (Nq + 3) & ~3;
   for (int e0 = 0; e0 < n; e0 += kBatch) {
@@ -371,8 +377,8 @@ __device__ __forceinline__ void interval(const uint32_t *keys, const float *rrow
 // CERTIFY = false: the selection on exact scores.  CERTIFY = true: `scores`
 // holds estimates with radii (CertArgs); the decisions the estimates cannot
 // settle are settled by recomputing fixed-order scores (see above).
-template <bool CERTIFY, int CH>
-__global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb_max,
+template <bool CERTIFY, int CH, int NT>
+__global__ void __launch_bounds__(NT) k_select(const float *scores, int Nb_max,
                                                      const int32_t *__restrict__ seq_len, int Hkv, int K, int W,
                                                      int cap, const int32_t *table_in, int32_t *table_out,
                                                      oasis_xfer_t *__restrict__ plan, int32_t *__restrict__ plan_count,
@@ -380,7 +386,8 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   extern __shared__ __align__(16) unsigned char smraw[];
   __shared__ SelScalars sc;
   __shared__ __align__(16) uint32_t hist[2][256];  // radix pass p counts into hist[p & 1]
-  __shared__ float red[4][kWarps];
+  __shared__ float red[4][kMaxWarps];
+  constexpr int kThreads = NT, kWarps = NT / 32;
   __shared__ int nX;
 
   const int s = blockIdx.x;
@@ -469,7 +476,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
   if constexpr (CERTIFY) {
     if (nc > K) {
       // T by the estimates, then the blocks it cannot settle
-      topk_bitmap<3>(keys, nc, K, bmT, hist, sc);
+      topk_bitmap<3, NT>(keys, nc, K, bmT, hist, sc);
       __syncthreads();
       float lo_in[1] = {INFINITY}, hi_out[1] = {-INFINITY};
       for (int b = tid; b < nc; b += kThreads) {
@@ -482,19 +489,19 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
           hi_out[0] = fmaxf(hi_out[0], hi);
       }
       if (tid == 0) nX = 0;  // read after the reduction's barriers
-      block_minmax<1>(lo_in, hi_out, red);
+      block_minmax<1, NT>(lo_in, hi_out, red);
       for (int b = tid; b < nc; b += kThreads) {
         float lo, hi;
         interval(keys, rrow, bmX, b, lo, hi);
         if (!(lo > hi_out[0]) && !(hi < lo_in[0])) xl[atomicAdd(&nX, 1)] = b;  // NaN lands here too
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
+      recompute_blocks<CH, NT>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
       // T = the settled members of the estimated T, and as many of the recomputed
       // ones as the estimated T held, best first by the exact keys
       int need = 0;
       for (int i = tid; i < nX; i += kThreads) need += bit(bmT, xl[i]);
-      need = block_sum(need, sc.warp_tot);
+      need = block_sum<NT>(need, sc.warp_tot);
       for (int i = warp; i < nX; i += kWarps) {
         const int b = xl[i];
         const uint64_t ci = composite(keys[b], b);
@@ -514,12 +521,12 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
       __syncthreads();
     }
   } else {
-    topk_bitmap<4>(keys, nc, K, bmT, hist, sc);
+    topk_bitmap<4, NT>(keys, nc, K, bmT, hist, sc);
     __syncthreads();
   }
   if constexpr (CERTIFY) {
     if (nc <= K) {
-      topk_bitmap<4>(keys, nc, K, bmT, hist, sc);  // every candidate
+      topk_bitmap<4, NT>(keys, nc, K, bmT, hist, sc);  // every candidate
       __syncthreads();
     }
   }
@@ -591,7 +598,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
           lo_[1] = fminf(lo_[1], lo);  // kept by the estimates
       }
       if (tid == 0) nX = 0;  // read after the reduction's barriers
-      block_minmax<2>(lo_, hi_, red);
+      block_minmax<2, NT>(lo_, hi_, red);
       const float a_lo = lo_[0], a_hi = hi_[0], e_lo = lo_[1], e_hi = hi_[1];
       for (int i = tid; i < nN && certA; i += kThreads) {
         const int b = composite_block(listN[i]);
@@ -606,7 +613,7 @@ __global__ void __launch_bounds__(kThreads) k_select(const float *scores, int Nb
         if (!bit(bmX, b) && !(lo > e_hi) && !(hi < e_lo)) xl[atomicAdd(&nX, 1)] = b;
       }
       __syncthreads();
-      recompute_blocks<CH>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
+      recompute_blocks<CH, NT>(xl, nX, gmin, gmax, Nb_max, Nq, qseg, ca.G, Hq_c, stage, res, srow_w, keys, bmX, sc);
       for (int i = tid; i < nN; i += kThreads) {
         const int b = composite_block(listN[i]);
         listN[i] = composite(keys[b], b);
@@ -700,19 +707,63 @@ size_t select_smem_bytes(int Nb_max, int K, int W, int cap) {
 }
 
 
+namespace {
+
+// Threads per selection CTA: 512 while every segment's CTA can have an SM to
+// itself, else 256, so that selection CTAs stay small enough to share SMs with
+// the scoring and attention CTAs of other layers (measured on GB300: 512-thread
+// CTAs cost the 256-segment decode step 13 us per layer-step; 256-thread CTAs
+// cost the 64- and 128-segment steps 0.7 and 2.5 us).
+int select_threads(int segments) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    sms = 0;
+  }
+  return segments <= sms ? 512 : 256;
+}
+
+template <int NT>
+cudaError_t launch_exact(const float *scores, int Nb_max, const int32_t *seq_len, int S, int Hkv, int K, int W,
+                         int cap, const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
+                         int32_t *plan_count, int32_t *status, size_t smem, cudaStream_t st) {
+  // static (histograms, scalars) + dynamic shared memory may pass the 48 KiB
+  // default before the dynamic part alone does
+  if (smem + kStaticSmemBound > 48 * 1024) {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select<false, 1, NT>), smem);
+    if (e != cudaSuccess) return e;
+  }
+  LaunchCfg lc(dim3(S), dim3(NT), smem, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_select<false, 1, NT>, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in,
+                            table_out, plan, plan_count, status, CertArgs{});
+}
+
+template <int CH, int NT>
+cudaError_t launch_cert(const float *scores, int Nb_max, const int32_t *seq_len, int S, int Hkv, int K, int W,
+                        int cap, const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
+                        int32_t *plan_count, int32_t *status, const CertArgs &ca, size_t smem, cudaStream_t st) {
+  if (smem + kStaticSmemBound > 48 * 1024) {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select<true, CH, NT>), smem);
+    if (e != cudaSuccess) return e;
+  }
+  LaunchCfg lc(dim3(S), dim3(NT), smem, st);
+  return cudaLaunchKernelEx(&lc.cfg, k_select<true, CH, NT>, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in,
+                            table_out, plan, plan_count, status, ca);
+}
+
+}  // namespace
+
 cudaError_t launch_select_topk_capped(const float *scores, int Nb_max, const int32_t *seq_len, int B, int Hkv,
                                       int K, int W, int cap, const int32_t *table_in, int32_t *table_out,
                                       oasis_xfer_t *plan, int32_t *plan_count, int32_t *status, cudaStream_t st) {
   const size_t smem = select_smem_bytes(Nb_max, K, W, cap);
-  // static (histograms, scalars) + dynamic shared memory may pass the 48 KiB
-  // default before the dynamic part alone does
-  if (smem + kStaticSmemBound > 48 * 1024) {
-    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_select<false, 1>), smem);
-    if (e != cudaSuccess) return e;
-  }
-  LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);
-  return cudaLaunchKernelEx(&lc.cfg, k_select<false, 1>, scores, Nb_max, seq_len, Hkv, K, W, cap, table_in,
-                            table_out, plan, plan_count, status, CertArgs{});
+  const int S = B * Hkv;
+  if (select_threads(S) == 512)
+    return launch_exact<512>(scores, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                             status, smem, st);
+  return launch_exact<256>(scores, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                           status, smem, st);
 }
 
 size_t select_tc_smem_bytes(int Nb_max, int K, int W, int cap, int D, int Nq) {
@@ -725,19 +776,19 @@ cudaError_t launch_select_topk_capped_tc(float *scores, const float *radius, con
                                          const int32_t *table_in, int32_t *table_out, oasis_xfer_t *plan,
                                          int32_t *plan_count, int32_t *status, cudaStream_t st) {
   const size_t smem = select_tc_smem_bytes(Nb_max, K, W, cap, D, G * Nd);
-  const void *fn = D == 128 ? reinterpret_cast<const void *>(k_select<true, 16>)
-                            : reinterpret_cast<const void *>(k_select<true, 8>);
-  if (smem + kStaticSmemBound > 48 * 1024) {
-    cudaError_t e = raise_smem_limit(fn, smem);
-    if (e != cudaSuccess) return e;
-  }
   const CertArgs ca{scores, radius, kmin, kmax, qdraft, G, Nd};
-  LaunchCfg lc(dim3(B * Hkv), dim3(kThreads), smem, st);
+  const int S = B * Hkv;
+  const float *sc = scores;
+  const bool wide = select_threads(S) == 512;
   if (D == 128)
-    return cudaLaunchKernelEx(&lc.cfg, k_select<true, 16>, static_cast<const float *>(scores), Nb_max, seq_len, Hkv,
-                              K, W, cap, table_in, table_out, plan, plan_count, status, ca);
-  return cudaLaunchKernelEx(&lc.cfg, k_select<true, 8>, static_cast<const float *>(scores), Nb_max, seq_len, Hkv, K,
-                            W, cap, table_in, table_out, plan, plan_count, status, ca);
+    return wide ? launch_cert<16, 512>(sc, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                                       status, ca, smem, st)
+                : launch_cert<16, 256>(sc, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                                       status, ca, smem, st);
+  return wide ? launch_cert<8, 512>(sc, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                                    status, ca, smem, st)
+              : launch_cert<8, 256>(sc, Nb_max, seq_len, S, Hkv, K, W, cap, table_in, table_out, plan, plan_count,
+                                    status, ca, smem, st);
 }
 
 }  // namespace oasis
