@@ -46,7 +46,7 @@ WORKLOAD_ID = 5
 def _args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30, help="decode steps timed (one graph replay each)")
+    p.add_argument("--steps", type=int, default=40, help="decode steps timed (one graph replay each)")
     p.add_argument("--warmup", type=int, default=5, help="decode steps run before timing")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=0,
