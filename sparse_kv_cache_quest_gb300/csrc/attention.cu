@@ -30,7 +30,9 @@
 // Warps combine through shared memory (reusing the rings), then every CTA of
 // the cluster combines a 1/CL share of the outputs from all CL CTAs' totals
 // through distributed shared memory and writes it to out and lse.  No global
-// scratch memory is used.
+// scratch memory is used.  With more than 8 query heads per KV head the heads
+// are split over warp pairs that share a partition's ring (k_attn_hs, further
+// down), so that each warp carries the math of 8 heads.
 //
 // k_attn_bal (further down) is the alternative split over all segments' slots
 // with a caller workspace; it measured slower than the cluster split on the

@@ -38,14 +38,18 @@
 //   warp 1, one lane  - D/16 MMAs per half-tile into one of four TMEM
 //                       accumulators (the warp also owns the TMEM allocation);
 //   warps 2-5 (scan)  - per segment, the split query operand {q+, q-} in the
-//                       no-swizzle K-major layout and Q_d (two buffers, built one
-//                       segment ahead); per half-tile, C_b's share from the stage
-//                       (each thread one block row), then the stage is released;
-//                       C_b goes to the TMEM warps through a small ring;
+//                       no-swizzle K-major layout, Q_d and max_d Q_d (two
+//                       buffers, built one segment ahead); without wrong-side
+//                       sums also, per half-tile, C_b's share from the stage
+//                       (each thread one block row), after which the stage is
+//                       released, and C_b to the TMEM warps through a small ring;
 //   warps 6-9 (TMEM)  - the accumulator row (tcgen05.ld), the max over the
-//                       columns, the radius, the stores.
+//                       columns, the radius (with wrong-side sums, C_b = max_d
+//                       Q_d * wsum_b from a load issued a tile ahead), the stores.
 // The scan warps move with the copies and the TMEM warps with the MMAs, so
-// neither holds up the other's ring.
+// neither holds up the other's ring; the tile walk and the ring positions are
+// kept as counters (a 64-bit division on the single MMA lane costs more than
+// the MMAs it issues).
 // Shared-memory operands use the no-swizzle K-major layout of 8-row x 16-byte
 // core matrices: the chunk-major summaries already are that layout (chunk c of
 // 128 blocks = 16 core matrices at 128-byte steps), so a half-tile lands as is:

@@ -15,7 +15,9 @@
 //   A in ascending id takes the freed slots (filled empties, then the slots of
 //   evicted residents) in ascending slot order.
 //
-// One CTA of 512 threads per segment, everything in shared memory:
+// One CTA per segment (512 threads while the segments do not outnumber the
+// SMs, else 256 so that the CTAs share SMs with other kernels), the working
+// set in shared memory:
 //  * scores -> order-preserving 32-bit keys (larger key = larger score; -0 is
 //    mapped to +0 so the two tie; NaN maps to 0, below -inf, and is flagged);
 //  * T by a 4-pass 8-bit MSB radix select of the K-th largest key (shared-
