@@ -27,8 +27,10 @@
 // is therefore identical to the selection on the fixed-order scores.
 //
 // Work split: the tiles (128 consecutive candidate blocks of one segment) of
-// all segments form one range, split evenly over a persistent grid of one CTA
-// per SM.  A tile is moved in two halves (its kmax chunks, then its kmin
+// all segments form one range, split evenly over a persistent grid of two CTAs
+// per SM (two MMA lanes and rings side by side: a lane blocks while its MMAs
+// run, and each CTA holds one query-operand buffer, rebuilt when its segment
+// changes).  A tile is moved in two halves (its kmax chunks, then its kmin
 // chunks; 32 KiB each at d_h 128) through a ring of half-tile stages.  Roles in
 // a CTA (warp-specialised, mbarrier hand-offs, every wait bounded):
 //   warp 0, one lane  - one 3-D TMA tensor copy per half-tile (a box of 16
@@ -38,8 +40,8 @@
 //   warp 1, one lane  - D/16 MMAs per half-tile into one of four TMEM
 //                       accumulators (the warp also owns the TMEM allocation);
 //   warps 2-5 (scan)  - per segment, the split query operand {q+, q-} in the
-//                       no-swizzle K-major layout, Q_d and max_d Q_d (two
-//                       buffers, built one segment ahead); without wrong-side
+//                       no-swizzle K-major layout, Q_d and max_d Q_d (built
+//                       once the previous segment's MMAs are done); without wrong-side
 //                       sums also, per half-tile, C_b's share from the stage
 //                       (each thread one block row), after which the stage is
 //                       released, and C_b to the TMEM warps through a small ring;
@@ -69,7 +71,9 @@ constexpr int kNAcc = 4;                      // TMEM accumulators
 constexpr int kNC = 4;                        // C_b hand-off ring (scan -> TMEM warps)
 constexpr uint32_t kChunkBytes = kRows * 16;  // one 8-dim chunk of a tile
 constexpr uint32_t kWaitTriesTC = 1u << 22;   // bounded mbarrier polls (far beyond any real copy or MMA)
-constexpr size_t kSmemCap = 227 * 1024;
+constexpr int kCtasPerSm = 2;                 // CTAs per SM: two MMA lanes and rings side by side
+constexpr int kBBufs = 1;                     // query-operand buffers per CTA
+constexpr size_t kSmemCap = (228 * 1024) / kCtasPerSm - 1024;  // per CTA (1 KiB of each SM's share is reserved)
 constexpr int kMaxStages = 8;
 
 // ---- tcgen05 / TMEM primitives (inline PTX, sm_100a family) -----------------
@@ -198,7 +202,7 @@ struct TileIter {
 };
 
 template <int N, int CH>
-__global__ void __launch_bounds__(kThreadsTC, 1)
+__global__ void __launch_bounds__(kThreadsTC, kCtasPerSm)
     k_score_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmn, bool use_tma,
                const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax,
                const float *__restrict__ wsum, int Nb_max, const uint16_t *__restrict__ qdraft, int S, int Hkv,
@@ -211,8 +215,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
   constexpr uint32_t kTmemCols = kNAcc * N <= 64 ? 64 : (kNAcc * N <= 128 ? 128 : 256);
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sA = smem;                                               // [stages][kHalf]
-  uint8_t *sB = sA + static_cast<size_t>(stages) * kHalf;           // [2][kBBytes]
-  float *sQ = reinterpret_cast<float *>(sB + 2 * kBBytes);          // [2][D]
+  uint8_t *sB = sA + static_cast<size_t>(stages) * kHalf;           // [kBBufs][kBBytes]
+  float *sQ = reinterpret_cast<float *>(sB + kBBufs * kBBytes);     // [2][D]
   float *sC = sQ + 2 * D;                                           // [kNC][kRows]
   float *sQmax = sC + kNC * kRows;                                  // [2]: max_d Q_d per query buffer
   uint64_t *bars = reinterpret_cast<uint64_t *>(sQmax + 2);
@@ -334,8 +338,8 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
         const int s = it.s;
         if (s != seg_prev) {  // the query operand of this segment
           if (seg_prev >= 0) tc_commit(&bqE[buf]);  // the previous segment's operand is free once its MMAs are done
-          buf = nseg & 1;
-          ok = wait_or_abort(&bqF[buf], static_cast<uint32_t>(nseg >> 1) & 1u, abort_flag);
+          buf = nseg % kBBufs;
+          ok = wait_or_abort(&bqF[buf], static_cast<uint32_t>(nseg / kBBufs) & 1u, abort_flag);
           ++nseg;
           seg_prev = s;
           if (!ok) break;
@@ -389,10 +393,10 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
     auto build_next = [&]() {
       while (next_build <= s_last && !it.active(next_build)) ++next_build;
       if (next_build > s_last) return;
-      const int s = next_build, bq = built & 1;
+      const int s = next_build, bq = built % kBBufs, qs = built & 1;  // operand buffer, Q / max slot
       const int bseq = s / Hkv, h = s % Hkv;
       uint8_t *B = sB + static_cast<size_t>(bq) * kBBytes;
-      float *Q = sQ + bq * D;
+      float *Q = sQ + qs * D;
       uint4 raw[kItems];
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {  // every load in flight before the first use
@@ -404,12 +408,12 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
               qdraft + ((static_cast<int64_t>(bseq) * Nd + jd) * Hq + h * G + g) * D + c * 8));
         }
       }
-      // the MMAs of the segment two back (same buffer) have completed (after an
-      // abort the wait returns at once; the outputs are then void anyway)
-      if (built >= 2) {
-        wait_or_abort(&bqE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
-        wait_or_abort(&qmE[bq], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
-      }
+      // the MMAs of the last segment that used this buffer have completed, and
+      // the TMEM warps took the max_d Q_d of the last that used this slot (after
+      // an abort the waits return at once; the outputs are then void anyway)
+      if (built >= kBBufs)
+        wait_or_abort(&bqE[bq], static_cast<uint32_t>((built / kBBufs) - 1) & 1u, abort_flag);
+      if (built >= 2) wait_or_abort(&qmE[qs], static_cast<uint32_t>((built >> 1) - 1) & 1u, abort_flag);
       scan_barrier();  // every scan thread is done with this buffer's previous segment
 #pragma unroll
       for (int k = 0; k < kItems; ++k) {
@@ -447,15 +451,14 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       if (et == 0) {
         float qm = 0.0f;
         for (int d = 0; d < D; ++d) qm = fmaxf(qm, Q[d]);
-        sQmax[bq] = qm;
-        mbar_arrive(&qmF[bq]);
+        sQmax[qs] = qm;
+        mbar_arrive(&qmF[qs]);
       }
       scan_barrier();
       ++next_build;
       ++built;
     };
-    build_next();
-    build_next();
+    for (int k = 0; k < kBBufs; ++k) build_next();  // the first segments' operands
     // The group never leaves these loops early: after an abort every wait returns
     // at once and the work is skipped, so all four warps meet at the same named
     // barriers (inside build_next) whatever happened.
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(kThreadsTC, 1)
       for (it.begin(); it.valid(); it.advance()) {
         const int s = it.s;
         if (s != seg_prev) {
-          if (seg_prev >= 0) build_next();  // the segment before is done: its buffer is rebuilt for the next-but-one
+          if (seg_prev >= 0) build_next();  // the segment before is done: its buffer takes the next unbuilt one
           bq = used & 1;
           ++used;
           seg_prev = s;
@@ -647,7 +650,7 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
   CUtensorMap tmx{}, tmn{};
   const bool use_tma = Nb_max % 8 == 0 && make_summary_map(&tmx, kmax, S, CH, Nb_max) == 0 &&
                        make_summary_map(&tmn, kmin, S, CH, Nb_max) == 0;
-  const size_t fixed = 2 * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
+  const size_t fixed = kBBufs * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
                        (2 * kMaxStages + 2 * kNAcc + 8 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kHalf));
   if (stages < 2) return cudaErrorInvalidValue;
@@ -656,7 +659,7 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score_tc<N, CH>), kThreadsTC, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t T = static_cast<int64_t>(S) * tps;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, T));
+  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(kCtasPerSm) * sms, T));
   LaunchCfg lc(dim3(grid), dim3(kThreadsTC), smem, st);
   return cudaLaunchKernelEx(&lc.cfg, k_score_tc<N, CH>, tmx, tmn, use_tma, kmin, kmax, wsum, Nb_max, qdraft, S,
                             Hkv, G, Nd, seq_len, W, scores, radius, status, tps, stages);
