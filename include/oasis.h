@@ -208,8 +208,8 @@ int oasis_score_blocks(const uint16_t *kmin, const uint16_t *kmax, int Nb_max, c
  *           wrong side of zero).
  * oasis_select_topk_capped_tc turns these into the exact selection.
  * Host-side checks, alignment and EINVAL cases: as oasis_score_blocks, plus
- * radius (4-byte aligned, not NULL).  One CTA per SM with about 200 KB of
- * shared memory; every internal wait is bounded (OASIS_STATUS_TIMEOUT).
+ * radius (4-byte aligned, not NULL).  Two CTAs per SM with up to 113 KB of
+ * shared memory each; every internal wait is bounded (OASIS_STATUS_TIMEOUT).
  */
 int oasis_score_blocks_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
                           const uint16_t *qdraft, int B, int Hkv, int G, int Nd, int D, const int32_t *seq_len, int W,
