@@ -63,8 +63,9 @@ def _args(argv=None):
     p.add_argument("--bg-streams", type=int, default=3, help="background streams, taken by the layers in turn")
     p.add_argument("--xf-streams", type=int, default=2, help="staging streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
-    p.add_argument("--attn", choices=["cluster", "balanced"], default="cluster",
-                   help="attention split: per-head thread-block clusters, or SM-balanced with a workspace")
+    p.add_argument("--attn", choices=["cluster", "balanced", "tc"], default="cluster",
+                   help="attention: per-head thread-block clusters (mma.sync), SM-balanced with a workspace, or the "
+                        "tcgen05 kernel (per-head clusters, both products on the 5th-generation tensor cores)")
     p.add_argument("--scoring", choices=["tc", "exact"], default="tc",
                    help="tc: tensor-core estimates + certified selection; exact: fixed-order fp32 scores of every "
                         "block (both give the same tables and plans)")
@@ -376,7 +377,7 @@ class Workbench:
     one synthetic layer, the pinned host tier, and the queries of every drift
     step.  reset() puts every layer back to the prior tables and pools."""
 
-    def __init__(self, w, R, dev, balanced_attn=False, scoring="tc"):
+    def __init__(self, w, R, dev, balanced_attn=False, scoring="tc", tc_attn=False):
         import torch
 
         import sparse_kv_cache_quest_gb300 as okv
@@ -396,7 +397,7 @@ class Workbench:
         self.strides = (tiles.stride(0), tiles.stride(1), tiles.stride(3))
         self.layers = []
         for _ in range(R):
-            lay = okv.DecodeLayer(shape, device=dev, balanced_attn=balanced_attn, scoring=scoring)
+            lay = okv.DecodeLayer(shape, device=dev, balanced_attn=balanced_attn, scoring=scoring, tc_attn=tc_attn)
             lay.build_summary(tiles, self.sl, 0, w.Nb, strides=self.strides)
             self.layers.append(lay)
         self.table0 = _gpu_prior(w, self.layers[0], self.sl, self.q[0]).to(dev)
@@ -490,7 +491,7 @@ def _kernel_times(wb, dev, n_rep=20):
     return kern
 
 
-def _roofline(w, kern, scoring="tc"):
+def _roofline(w, kern, scoring="tc", attn="cluster"):
     peak, peak_kind = _peaks()
     fp32_peak = _fp32_peak_tfma()
     score_bytes = w.summary_bytes_per_layer()
@@ -499,7 +500,7 @@ def _roofline(w, kern, scoring="tc"):
     score_fma = w.S * w.nc * w.Nq * w.D
     k_gbs = {"score": score_bytes / (kern["score"] * 1e-6) / 1e9, "attn": attn_bytes / (kern["attn"] * 1e-6) / 1e9}
     dom = "attn" if kern["attn"] >= kern["score"] else "score"
-    kname = {"attn": "k_attn", "score": "k_score_tc" if scoring == "tc" else "k_score"}
+    kname = {"attn": "k_attn_tc" if attn == "tc" else "k_attn", "score": "k_score_tc" if scoring == "tc" else "k_score"}
     sname = ("k_score_tc (oasis_score_blocks_tc, tensor cores)" if scoring == "tc"
              else "k_score (oasis_score_blocks)")
     score_tfma = score_fma / (kern["score"] * 1e-6) / 1e12
@@ -522,10 +523,12 @@ def _roofline(w, kern, scoring="tc"):
         roof = {"kernel": sname, "bound": "alu", **score_fp32,
                 "traffic": _traffic("k_score", w), "timing": timing,
                 "other": {"attn": {"us": kern["attn"], "gbs": k_gbs["attn"], "frac": k_gbs["attn"] / peak,
-                                   "traffic": _traffic("k_attn", w)},
+                                   "traffic": _traffic(kname["attn"], w)},
                           "score_hbm": {"gbs": k_gbs["score"], "frac": k_gbs["score"] / peak}}}
     else:
-        roof = {"kernel": {"attn": "k_attn (oasis_sparse_decode_attn)", "score": sname}[dom],
+        aname = ("k_attn_tc (oasis_sparse_decode_attn_tc, tcgen05)" if attn == "tc"
+                 else "k_attn (oasis_sparse_decode_attn)")
+        roof = {"kernel": {"attn": aname, "score": sname}[dom],
                 "bound": "hbm", "achieved": k_gbs[dom], "peak": peak, "unit": "GB/s", "frac": k_gbs[dom] / peak,
                 "peak_kind": pk, "traffic": _traffic(kname[dom], w),
                 "algorithmic_bytes_per_launch": attn_bytes if dom == "attn" else score_bytes, "timing": timing,
@@ -567,7 +570,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # ---- setup (untimed): KV cache, summaries, prior tables, pools, pinned host tier
-    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring)
+    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring, tc_attn=args.attn == "tc")
     graphs = wb.graphs(args)
     wb.reset()                                  # the capture's warm-up ran one step: start from the prior again
 
@@ -642,7 +645,7 @@ def run_ours(args):
                 "gpu_launches": 5 * R * K,
                 "e2e": e2e, "cpu_baseline": cpu, "clocks": clk}
         if kern is not None:
-            line["roofline"] = _roofline(w, kern, args.scoring)
+            line["roofline"] = _roofline(w, kern, args.scoring, args.attn)
             line["kernels_us"] = kern
         if others:
             line["other_workloads"] = others
@@ -682,7 +685,7 @@ def _other_workload(args, wid, dev, steps=10, warmup=3):
     from synth import workload as wl
     w = wl.WORKLOADS[wid]
     R = w.layers if w.layers > 1 else 36
-    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring)
+    wb = Workbench(w, R, dev, balanced_attn=args.attn == "balanced", scoring=args.scoring, tc_attn=args.attn == "tc")
     graphs = wb.graphs(args)
     wb.reset()
     for i in range(warmup):
@@ -692,7 +695,7 @@ def _other_workload(args, wid, dev, steps=10, warmup=3):
     st = wb.status()
     assert st == 0, st
     kern = _kernel_times(wb, dev)
-    roof = _roofline(w, kern, args.scoring)
+    roof = _roofline(w, kern, args.scoring, args.attn)
     out = {"workload": _config(w, R)["workload"], "layers": R, "us_per_layer_step": ms * 1e3 / R,
            "value_gbs": w.headline_bytes_per_layer() / (ms * 1e-3 / R) / 1e9, "steps": steps,
            "kernels_us": kern,

@@ -18,7 +18,8 @@
  *   oasis_stage_blocks        host-resident KV tiles -> HBM slots (the plan)
  *   oasis_sparse_decode_attn  attention of the true query over the slots
  *                             (oasis_sparse_decode_attn_ws: SM-balanced, with a
- *                             caller workspace)
+ *                             caller workspace; oasis_sparse_decode_attn_tc:
+ *                             both products on the tcgen05 tensor cores)
  * and the tensor-core scoring path that replaces the second and third calls
  * with the same selections:
  *   oasis_score_blocks_tc        score estimates with certified error radii
@@ -105,7 +106,7 @@ extern "C" {
 /* cudaStream_t without including the CUDA headers (it is this same type). */
 typedef struct CUstream_st *oasis_stream_t;
 
-#define OASIS_ABI_VERSION 2
+#define OASIS_ABI_VERSION 3
 
 /* Return codes. */
 #define OASIS_OK 0
@@ -358,6 +359,23 @@ int oasis_sparse_decode_attn_ws(const uint16_t *q, const uint16_t *pool, const i
 int oasis_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, const int32_t *table,
                                      int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G, int D,
                                      float scale, float *out, float *lse, int32_t *status, oasis_stream_t stream);
+
+/*
+ * The same attention with both products on the tcgen05 tensor cores (the
+ * calls above use warp-level mma.sync): per CTA, tiles of 8 slots (128
+ * tokens) land by TMA; S^T = K . Q^T and O^T = V^T . P^T (P as a bf16 hi + lo
+ * pair) run as tcgen05 MMAs into tensor memory, and the softmax warps read S
+ * and O back from it.  A segment is split over a cluster of up to 4 CTAs as in
+ * oasis_sparse_decode_attn.  Same arguments, outputs, status bits and error
+ * bound.  Alone it matches the mma.sync kernel on 16 query heads per KV head
+ * and is slower on 4; its 113 KB CTAs leave no room beside them for the
+ * selection and staging kernels of a layer-pipelined step, so it is not the
+ * default.
+ * EINVAL: as oasis_sparse_decode_attn, or D not 128.
+ */
+int oasis_sparse_decode_attn_tc(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
+                                const int32_t *seq_len, int B, int Hkv, int G, int D, float scale,
+                                float *out, float *lse, int32_t *status, oasis_stream_t stream);
 
 #ifdef __cplusplus
 }

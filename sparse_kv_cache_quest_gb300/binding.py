@@ -25,6 +25,7 @@ EXPORTS = (
     "oasis_strerror", "oasis_abi_version", "oasis_build_summary", "oasis_score_blocks", "oasis_score_blocks_tc",
     "oasis_select_topk_capped", "oasis_select_topk_capped_tc", "oasis_stage_blocks", "oasis_sparse_decode_attn",
     "oasis_attn_workspace_bytes", "oasis_sparse_decode_attn_ws", "oasis_sparse_decode_attn_noalloc",
+    "oasis_sparse_decode_attn_tc",
 )
 
 
@@ -60,6 +61,7 @@ _SIGS = {
     "oasis_sparse_decode_attn_ws": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, ctypes.c_size_t, _P,
                                          _P]),
     "oasis_sparse_decode_attn_noalloc": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
+    "oasis_sparse_decode_attn_tc": (_I, [_P, _P, _P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P]),
 }
 
 
@@ -176,6 +178,13 @@ def oasis_sparse_decode_attn_ws(q, pool, table, slots_per_seg, seq_len, B, Hkv, 
 def oasis_sparse_decode_attn_noalloc(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse=None,
                                      status=None, stream=None):
     return _check("oasis_sparse_decode_attn_noalloc", load().oasis_sparse_decode_attn_noalloc(
+        _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
+        _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
+
+
+def oasis_sparse_decode_attn_tc(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse=None,
+                                status=None, stream=None):
+    return _check("oasis_sparse_decode_attn_tc", load().oasis_sparse_decode_attn_tc(
         _ptr(q), _ptr(pool), _ptr(table), slots_per_seg, _ptr(seq_len), B, Hkv, G, D, float(scale),
         _ptr(out), _ptr(lse), _ptr(status), _stream(stream)))
 

@@ -261,4 +261,18 @@ int oasis_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, co
                                                          scale, out, lse, status, stream));
 }
 
+int oasis_sparse_decode_attn_tc(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
+                                const int32_t *seq_len, int B, int Hkv, int G, int D, float scale, float *out,
+                                float *lse, int32_t *status, oasis_stream_t stream) {
+  if (!q || !pool || !table || !seq_len || !out) return OASIS_EINVAL;
+  if (D != 128 || !segs_ok(B, Hkv) || G < 1 || G > 16 || slots_per_seg < 1 || slots_per_seg > 4096)
+    return OASIS_EINVAL;
+  if (static_cast<int64_t>(B) * Hkv * slots_per_seg * 32 > 0x7FFFFFFF) return OASIS_EINVAL;  // pool rows
+  if (!aligned16(q) || !aligned16(pool) || !aligned4(table) || !aligned4(seq_len) || !aligned4(out))
+    return OASIS_EINVAL;
+  if ((lse && !aligned4(lse)) || (status && !aligned4(status))) return OASIS_EINVAL;
+  return finish(oasis::launch_attn_tc(q, pool, table, slots_per_seg, seq_len, B, Hkv, G, D, scale, out, lse, status,
+                                      stream));
+}
+
 }  // extern "C"

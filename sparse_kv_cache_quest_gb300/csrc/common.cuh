@@ -163,6 +163,10 @@ cudaError_t launch_stage_blocks(const void *host_kv, int64_t host_seg_stride_byt
 cudaError_t launch_sparse_decode_attn(const uint16_t *q, const uint16_t *pool, const int32_t *table,
                                       int slots_per_seg, const int32_t *seq_len, int B, int Hkv, int G, int D,
                                       float scale, float *out, float *lse, int32_t *status, cudaStream_t st);
+bool attn_tc_supports(int G, int D);
+cudaError_t launch_attn_tc(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
+                           const int32_t *seq_len, int B, int Hkv, int G, int D, float scale, float *out, float *lse,
+                           int32_t *status, cudaStream_t st);
 size_t attn_workspace_bytes(int B, int Hkv, int G, int D, int slots_per_seg);
 size_t noalloc_scratch_bytes();
 cudaError_t launch_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, const int32_t *table,

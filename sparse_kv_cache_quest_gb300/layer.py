@@ -56,6 +56,8 @@ class DecodeLayer:
     balanced_attn: run the attention as the SM-balanced split with a workspace
     of this layer's own (oasis_sparse_decode_attn_ws) instead of the per-head
     cluster split (oasis_sparse_decode_attn).
+    tc_attn: run the attention on the tcgen05 tensor cores
+    (oasis_sparse_decode_attn_tc; d_h 128 only).
     scoring: "exact" - every score in the fixed-order fp32 arithmetic
     (oasis_score_blocks, then oasis_select_topk_capped); "tc" - tensor-core
     estimates with radii (oasis_score_blocks_tc), then the certified selection
@@ -63,7 +65,11 @@ class DecodeLayer:
     decisions need.  Both give the same tables and plans; with "tc" the scores
     buffer holds fixed-order values only for the recomputed blocks."""
 
-    def __init__(self, shape: LayerShape, device="cuda", balanced_attn: bool = False, scoring: str = "exact"):
+    def __init__(self, shape: LayerShape, device="cuda", balanced_attn: bool = False, scoring: str = "exact",
+                 tc_attn: bool = False):
+        if balanced_attn and tc_attn:
+            raise ValueError("balanced_attn and tc_attn are alternatives")
+        self.tc_attn = tc_attn
         self.shape = sh = shape
         dev = torch.device(device)
         self.device = dev
@@ -139,8 +145,9 @@ class DecodeLayer:
                                            self.scale, self.out, self.lse, self.attn_ws, self.attn_ws.numel(),
                                            self.status, stream)
             return
-        ob.oasis_sparse_decode_attn(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D,
-                                    self.scale, self.out, self.lse, self.status, stream)
+        fn = ob.oasis_sparse_decode_attn_tc if self.tc_attn else ob.oasis_sparse_decode_attn
+        fn(q, self.pool, self.table, sh.slots, seq_len, sh.B, sh.Hkv, sh.G, sh.D, self.scale, self.out, self.lse,
+           self.status, stream)
 
     def swap_tables(self):
         self.table, self.table_next = self.table_next, self.table

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(ob.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
-    assert okv.abi_version() == 2
+    assert okv.abi_version() == 3
 
 
 def test_strerror(lib):
@@ -116,3 +116,8 @@ def test_stage_and_attention_validation(lib):
     _einval(okv.oasis_sparse_decode_attn, P, P, P, 8, P, 1, 1, 0, 128, 0.1, P, None, None, 0)  # G
     _einval(okv.oasis_sparse_decode_attn, P, P, P, 0, P, 1, 1, 4, 128, 0.1, P, None, None, 0)  # slots
     _einval(okv.oasis_sparse_decode_attn, P + 8, P, P, 8, P, 1, 1, 4, 128, 0.1, P, None, None, 0)  # q align
+    f = okv.oasis_sparse_decode_attn_tc
+    _einval(f, P, P, P, 8, P, 1, 1, 4, 64, 0.1, P, None, None, 0)        # D 64: the tcgen05 kernel takes d_h 128
+    _einval(f, P, P, P, 8, P, 1, 1, 17, 128, 0.1, P, None, None, 0)      # G
+    _einval(f, P, P + 8, P, 8, P, 1, 1, 4, 128, 0.1, P, None, None, 0)   # pool not 16-byte aligned
+    _einval(f, P, P, None, 8, P, 1, 1, 4, 128, 0.1, P, None, None, 0)    # NULL table

@@ -28,11 +28,15 @@ def test_device_generator_matches_cpu():
 
 
 # the tensor-core scoring pair at 64 and 256 segments: the second runs the selection
-# at the width it takes when the segments outnumber the SMs
+# at the width it takes when the segments outnumber the SMs; "tc+attn" adds the
+# tcgen05 attention (clusters of 4 CTAs at 64 segments, 2 at 128, one CTA at 256)
 @pytest.mark.parametrize("cfg,scoring", [(1, "exact"), (2, "exact"), (3, "exact"), (4, "exact"), (5, "exact"),
-                                         (2, "tc"), (3, "tc"), (5, "tc")])
+                                         (2, "tc"), (3, "tc"), (5, "tc"),
+                                         (2, "tc+attn"), (4, "tc+attn"), (5, "tc+attn")])
 def test_workload_layer_parity(cfg, scoring):
     okv.load()
+    tc_attn = scoring == "tc+attn"
+    scoring = "tc" if tc_attn else scoring
     w = wl.WORKLOADS[cfg]
     layer = 0
     segs = sample_segments(w)
@@ -43,7 +47,7 @@ def test_workload_layer_parity(cfg, scoring):
     host = torch.empty(tiles.shape, dtype=torch.bfloat16).pin_memory()
     host.copy_(tiles)
 
-    lay = okv.DecodeLayer(_shape(w), scoring=scoring)
+    lay = okv.DecodeLayer(_shape(w), scoring=scoring, tc_attn=tc_attn)
     sl = seq_len.cuda()
     lay.build_summary(tiles, sl, 0, w.Nb, strides=(tiles.stride(0), tiles.stride(1), tiles.stride(3)))
     lay.table.copy_(table0.cuda())
