@@ -108,8 +108,11 @@ struct Plan {
   static constexpr int kLists = kBars + 8 * kWarps * kNST; // kWarps * kListMax int32
   static constexpr int kEnd = kLists + 4 * kWarps * kListMax;
   // combine scratch (floats), aliased onto the ring once every stage is drained
+  // (per-warp output rows padded to D + 4 floats: the fragment-order stores of
+  // lanes with different t then fall in different banks)
+  static constexpr int kOS = D + 4;
   static constexpr int kWarpM = 0, kWarpL = kWarps * GQ, kWarpO = 2 * kWarps * GQ;
-  static constexpr int kCtaM = kWarpO + kWarps * GQ * D, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
+  static constexpr int kCtaM = kWarpO + kWarps * GQ * kOS, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
   static constexpr int kScratchBytes = 4 * (kCtaO + GQ * D);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
@@ -348,7 +351,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int qc = nt * 8 + 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
-        wo[(warp * GQ + qc) * D + dim] = o[nt][mt][i];
+        wo[(warp * GQ + qc) * P::kOS + dim] = o[nt][mt][i];
       }
   }
   __syncthreads();
@@ -362,9 +365,15 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float f = exp2f(wm[w * GQ + qc] - M);
-        acc += f * wo[(w * GQ + qc) * D + d];
+        acc += f * wo[(w * GQ + qc) * P::kOS + d];
         ls += f * wl[w * GQ + qc];
       }
+    }
+    if (CL == 1) {  // one CTA: its totals are the results (the cluster merge would scale them by 2^0)
+      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
+      out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
+      if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+      continue;
     }
     co[qc * D + d] = acc;
     if (d == 0) {
@@ -372,6 +381,7 @@ __global__ void __launch_bounds__(kThreads)
       cl[qc] = ls;
     }
   }
+  if (CL == 1) return;  // no other CTA reads this one's shared memory
   cluster.sync();
   // Cluster merge: every rank combines its share of the G*D outputs, reading all
   // ranks' CTA totals through distributed shared memory with a thread's remote
@@ -439,8 +449,9 @@ struct PlanHS {
   static constexpr int kLists = kEmpty + 8 * kPairs * kNS;   // kWarpsHS * kListMax int32
   static constexpr int kEnd = kLists + 4 * kWarpsHS * kListMax;
   // combine scratch (floats): each warp's 8 heads (m, l, o), then the CTA's 16
+  static constexpr int kOS = D + 4;  // padded per-warp output rows, as in Plan
   static constexpr int kWarpM = 0, kWarpL = kWarpsHS * 8, kWarpO = 2 * kWarpsHS * 8;
-  static constexpr int kCtaM = kWarpO + kWarpsHS * 8 * D, kCtaL = kCtaM + 16, kCtaO = kCtaL + 16;
+  static constexpr int kCtaM = kWarpO + kWarpsHS * 8 * kOS, kCtaL = kCtaM + 16, kCtaO = kCtaL + 16;
   static constexpr int kScratchBytes = 4 * (kCtaO + 16 * D);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
@@ -609,7 +620,7 @@ __global__ void __launch_bounds__(kThreadsHS)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int qc = 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
-      wo[(warp * 8 + qc) * D + dim] = o[0][mt][i];
+      wo[(warp * 8 + qc) * P::kOS + dim] = o[0][mt][i];
     }
   __syncthreads();
   // head qc = 8 * half + j was processed by warps half * kPairs + p, p = 0..kPairs-1
@@ -625,9 +636,15 @@ __global__ void __launch_bounds__(kThreadsHS)
 #pragma unroll
       for (int p = 0; p < kPairs; ++p) {
         const float f = exp2f(wm[(w0 + p) * 8 + j] - M);
-        acc += f * wo[((w0 + p) * 8 + j) * D + d];
+        acc += f * wo[((w0 + p) * 8 + j) * P::kOS + d];
         ls += f * wl[(w0 + p) * 8 + j];
       }
+    }
+    if (CL == 1) {  // one CTA: its totals are the results (the cluster merge would scale them by 2^0)
+      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
+      out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
+      if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+      continue;
     }
     co[qc * D + d] = acc;
     if (d == 0) {
@@ -635,6 +652,7 @@ __global__ void __launch_bounds__(kThreadsHS)
       cl[qc] = ls;
     }
   }
+  if (CL == 1) return;  // no other CTA reads this one's shared memory
   cluster.sync();
   // cluster merge, as in k_attn
   {
@@ -846,7 +864,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int qc = nt * 8 + 2 * t + (i & 1), dim = 16 * mt + g + 8 * (i >> 1);
-          wo[(warp * GQ + qc) * D + dim] = o[nt][mt][i];
+          wo[(warp * GQ + qc) * PL::kOS + dim] = o[nt][mt][i];
         }
     }
     __syncthreads();
@@ -860,7 +878,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float f = exp2f(wm[w * GQ + qc] - M);
-          acc += f * wo[(w * GQ + qc) * D + d];
+          acc += f * wo[(w * GQ + qc) * PL::kOS + d];
           ls += f * wl[w * GQ + qc];
         }
       }
