@@ -72,6 +72,7 @@ constexpr int kNC = 4;                        // C_b hand-off ring (scan -> TMEM
 constexpr uint32_t kChunkBytes = kRows * 16;  // one 8-dim chunk of a tile
 constexpr uint32_t kWaitTriesTC = 1u << 22;   // bounded mbarrier polls (far beyond any real copy or MMA)
 constexpr int kCtasPerSm = 2;                 // CTAs per SM: two MMA lanes and rings side by side
+constexpr int kMaxRegsTC = 80;                // registers a thread (see the kernel)
 constexpr int kBBufs = 1;                     // query-operand buffers per CTA
 constexpr size_t kSmemCap = (228 * 1024) / kCtasPerSm - 1024;  // per CTA (1 KiB of each SM's share is reserved)
 constexpr int kMaxStages = 8;
@@ -202,7 +203,11 @@ struct TileIter {
 };
 
 template <int N, int CH>
-__global__ void __launch_bounds__(kThreadsTC, kCtasPerSm)
+// 80 registers a thread (no spills): two CTAs then take 51,200 of an SM's
+// 65,536, which leaves room on the same SM for a selection or a staging CTA of
+// another layer (at 96 they took 61,440 and any such CTA cost the SM one of its
+// scoring CTAs, started a wave late)
+__global__ void __maxnreg__(kMaxRegsTC)
     k_score_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmn, bool use_tma,
                const uint16_t *__restrict__ kmin, const uint16_t *__restrict__ kmax,
                const float *__restrict__ wsum, int Nb_max, const uint16_t *__restrict__ qdraft, int S, int Hkv,
