@@ -367,10 +367,10 @@ int oasis_sparse_decode_attn_noalloc(const uint16_t *q, const uint16_t *pool, co
  * pair) run as tcgen05 MMAs into tensor memory, and the softmax warps read S
  * and O back from it.  A segment is split over a cluster of up to 4 CTAs as in
  * oasis_sparse_decode_attn.  Same arguments, outputs, status bits and error
- * bound.  Alone it matches the mma.sync kernel on 16 query heads per KV head
- * and is slower on 4; its 113 KB CTAs leave no room beside them for the
- * selection and staging kernels of a layer-pipelined step, so it is not the
- * default.
+ * bound.  It is slower than the mma.sync kernels (it keeps a whole tile's
+ * values in shared memory through the softmax, so each CTA looks one tile
+ * ahead), and its 113 KB CTAs leave no room beside them for the selection and
+ * staging kernels of a layer-pipelined step, so it is not the default.
  * EINVAL: as oasis_sparse_decode_attn, or D not 128.
  */
 int oasis_sparse_decode_attn_tc(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots_per_seg,
