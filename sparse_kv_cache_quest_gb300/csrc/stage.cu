@@ -11,8 +11,18 @@
 // entries (segment-major) with a stride, one tile per warp at a time, all of
 // the tile's 16-byte loads issued before its stores.  That keeps about a
 // megabyte in flight, several times what the link needs to stay busy, in CTAs
-// of about 10k registers, so a staging CTA fits on an SM beside the CTAs of the
-// scoring or attention kernels that run on other streams.
+// of about 10k registers.
+//
+// Placement: a staging CTA holds some two thousand host loads outstanding in
+// its SM's load path for tens of microseconds, and on an SM that also runs two
+// CTAs of the head-split attention (whose warps are chains of dependent shared
+// memory loads and MMAs) it slows them.  The launch therefore reserves
+// kReserveSmem of shared memory that the kernel does not use: the block
+// scheduler then places a staging CTA only on an SM with room beside at most
+// one CTA of the streaming kernels (two 84 KB attention or 102 KB scoring CTAs
+// leave less than that).  Measured on the 235B-shaped decode step: 99.7 / 100.4
+// -> 96.9 / 97.1 us per layer-step; no change on the 4-head layers, whose 73 KB
+// attention CTAs still leave room.
 
 #include <algorithm>
 
@@ -25,6 +35,7 @@ constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCtas = 32;
 constexpr int kMaxPerLane = 16;  // 16-byte loads per lane for one tile at D = 128
+constexpr size_t kReserveSmem = 60 * 1024;  // shared memory reserved, not used (placement, above)
 
 __global__ void __launch_bounds__(kThreads) k_stage(const unsigned char *__restrict__ host, int64_t seg_stride,
                                                     int host_nb, const oasis_xfer_t *__restrict__ plan,
@@ -68,7 +79,9 @@ cudaError_t launch_stage_blocks(const void *host_kv, int64_t host_seg_stride_byt
   const int S = B * Hkv;
   const int64_t warps_needed = static_cast<int64_t>(S) * cap;
   const int grid = static_cast<int>(std::min<int64_t>(kCtas, (warps_needed + kWarps - 1) / kWarps));
-  LaunchCfg lc(dim3(grid), dim3(kThreads), 0, st);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(k_stage), kReserveSmem);
+  if (e != cudaSuccess) return e;
+  LaunchCfg lc(dim3(grid), dim3(kThreads), kReserveSmem, st);
   return cudaLaunchKernelEx(&lc.cfg, k_stage, static_cast<const unsigned char *>(host_kv), host_seg_stride_bytes,
                             host_nb, plan, plan_count, cap, S, D, pool, slots_per_seg, status);
 }
