@@ -367,6 +367,21 @@ __device__ void recompute_blocks(const int32_t *xl, int n, const uint4 *gmin, co
   }
 }
 
+// Rank of every entry of a list of distinct 64-bit keys: the number of larger
+// (kDesc) or smaller entries.  One thread per entry reads the whole list; all
+// threads of a warp read the same entry at a time (a broadcast), so a short list
+// costs a few hundred cycles where a warp-wide ballot per entry costs thousands.
+template <int NT, bool kDesc>
+__device__ __forceinline__ void rank_list(const uint64_t *list, int n, int32_t *rank) {
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint64_t ci = list[i];
+    int r = 0;
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) r += kDesc ? (list[j] > ci) : (list[j] < ci);
+    rank[i] = r;
+  }
+}
+
 // interval of block b from its key and radius (a recomputed block has radius 0)
 __device__ __forceinline__ void interval(const uint32_t *keys, const float *rrow, const uint32_t *bmX, int b,
                                          float &lo, float &hi) {
@@ -561,24 +576,8 @@ __global__ void __launch_bounds__(NT) k_select(const float *scores, int Nb_max,
     // estimates' intervals, recompute what they cannot settle
     const bool certA = nN > nA, certE = nEvict > 0 && nE > nEvict;
     if (certA || certE) {
-      for (int i = warp; i < nN; i += kWarps) {  // rank by the estimates (larger first)
-        const uint64_t ci = listN[i];
-        int r = 0;
-        for (int j0 = 0; j0 < nN; j0 += 32) {
-          const int j = j0 + lane;
-          r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && listN[j] > ci));
-        }
-        if (lane == 0) rankN[i] = r;
-      }
-      for (int i = warp; i < nE; i += kWarps) {  // rank from the bottom (smaller first)
-        const uint64_t ci = listE[i];
-        int r = 0;
-        for (int j0 = 0; j0 < nE; j0 += 32) {
-          const int j = j0 + lane;
-          r += __popc(__ballot_sync(0xFFFFFFFFu, j < nE && listE[j] < ci));
-        }
-        if (lane == 0) rankE[i] = r;
-      }
+      rank_list<NT, true>(listN, nN, rankN);   // rank by the estimates (larger first)
+      rank_list<NT, false>(listE, nE, rankE);  // rank from the bottom (smaller first)
       __syncthreads();
       // lo[0]/hi[0]: min over A~ / max over N \ A~; lo[1]/hi[1]: min over the kept
       // of E / max over the evicted of E
@@ -629,25 +628,14 @@ __global__ void __launch_bounds__(NT) k_select(const float *scores, int Nb_max,
   }
 
   // 5. A = the nA best of N; freed slots = first nFill empty slots + the nEvict worst of E.
-  // Every rank is a count over a list of at most K entries: one warp per entry,
-  // its lanes splitting the list, a ballot-popcount per 32 entries.
-  for (int i = warp; i < nN; i += kWarps) {
-    const uint64_t ci = listN[i];
-    int r = 0;
-    for (int j0 = 0; j0 < nN; j0 += 32) {
-      const int j = j0 + lane;
-      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && listN[j] > ci));
-    }
-    if (lane == 0) rankN[i] = r;
-  }
-  for (int i = warp; i < nE; i += kWarps) {
+  // Every rank is a count over a list of at most K entries (one thread per entry).
+  rank_list<NT, true>(listN, nN, rankN);
+  for (int i = tid; i < nE; i += kThreads) {
     const uint64_t ci = listE[i];
     int r = 0;
-    for (int j0 = 0; j0 < nE; j0 += 32) {
-      const int j = j0 + lane;
-      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nE && listE[j] < ci));
-    }
-    if (lane == 0 && r < nEvict) {
+#pragma unroll 4
+    for (int j = 0; j < nE; ++j) r += listE[j] < ci;
+    if (r < nEvict) {
       const int f = atomicAdd(&sc.nF, 1);
       if (f < cap) fList[f] = slotE[i];
     }
@@ -667,15 +655,12 @@ __global__ void __launch_bounds__(NT) k_select(const float *scores, int Nb_max,
     }
   }
   __syncthreads();
-  for (int i = warp; i < nN; i += kWarps) {
-    if (rankN[i] >= nA) continue;  // warp-uniform
+  for (int i = tid; i < nN; i += kThreads) {
+    if (rankN[i] >= nA) continue;
     const int b = composite_block(listN[i]);
     int r = 0;
-    for (int j0 = 0; j0 < nN; j0 += 32) {
-      const int j = j0 + lane;
-      r += __popc(__ballot_sync(0xFFFFFFFFu, j < nN && rankN[j] < nA && composite_block(listN[j]) < b));
-    }
-    if (lane == 0 && r < cap) aSorted[r] = b;
+    for (int j = 0; j < nN; ++j) r += rankN[j] < nA && composite_block(listN[j]) < b;
+    if (r < cap) aSorted[r] = b;
   }
   for (int i = tid; i < nA; i += kThreads) {
     const int sl = fList[i];
