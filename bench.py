@@ -61,7 +61,7 @@ def _args(argv=None):
     p.add_argument("--other-workloads", default="2,3",
                    help="workload ids also measured (layer-step and kernels, under other_workloads; '' for none)")
     p.add_argument("--bg-streams", type=int, default=3, help="background streams, taken by the layers in turn")
-    p.add_argument("--xf-streams", type=int, default=2, help="staging streams, taken by the layers in turn")
+    p.add_argument("--xf-streams", type=int, default=3, help="staging streams, taken by the layers in turn")
     p.add_argument("--fg-priority", type=int, default=0, help="CUDA priority of the foreground stream (lower = higher)")
     p.add_argument("--attn", choices=["cluster", "balanced", "tc"], default="cluster",
                    help="attention: per-head thread-block clusters (mma.sync), SM-balanced with a workspace, or the "

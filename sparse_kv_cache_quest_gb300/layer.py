@@ -305,7 +305,7 @@ class DecodeStepGraph:
 
     def __init__(self, layers, q, qdraft, seq_len, host_kv, host_seg_stride_bytes, host_nb, new_keys=None,
                  new_block: Optional[int] = None, host_io: bool = False, n_bg: int = 3, fg_priority: int = 0,
-                 n_xf: int = 2, advance: bool = False, share_host_inputs: bool = False, warmup: bool = True):
+                 n_xf: int = 3, advance: bool = False, share_host_inputs: bool = False, warmup: bool = True):
         dev = layers[0].device
         self.layers = layers
         self.seq_len = seq_len.detach().to(dev).clone()
@@ -327,10 +327,10 @@ class DecodeStepGraph:
         self.host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in x] for x in outs] \
             if host_io else None
         fg = torch.cuda.Stream(dev, priority=fg_priority)
-        # staging streams taken by alternate layers: the staging of layer l+1 may
-        # start while layer l's still runs, hiding each copy's start-up and tail
-        # behind its neighbour (the copies are bound by the host link, and a
-        # chain of them on one stream comes close to the step's critical path)
+        # staging streams taken by the layers in turn (three by default): the
+        # staging of layer l+1 may start while layer l's still runs, hiding each
+        # copy's start-up and tail behind its neighbours (the copies are bound by
+        # the host link, and a chain of them on one stream sets the step's pace)
         xfs = [torch.cuda.Stream(dev) for _ in range(n_xf)]
         # host I/O on copy streams of its own, per layer, so that the copies of one
         # layer overlap the kernels of the others
