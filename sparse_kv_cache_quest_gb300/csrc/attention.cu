@@ -29,8 +29,9 @@
 // whole output elements, so no cross-lane reduction is needed per slot.
 // Warps combine through shared memory (reusing the rings), then every CTA of
 // the cluster combines a 1/CL share of the outputs from all CL CTAs' totals
-// through distributed shared memory and writes it to out and lse.  No global
-// scratch memory is used.  With more than 8 query heads per KV head the heads
+// through distributed shared memory and writes it to out and lse; a segment
+// on one CTA (CL = 1) writes its outputs straight from the warp merge, with no
+// cluster barrier.  No global scratch memory is used.  With more than 8 query heads per KV head the heads
 // are split over warp pairs that share a partition's ring (k_attn_hs, further
 // down), so that each warp carries the math of 8 heads.
 //
