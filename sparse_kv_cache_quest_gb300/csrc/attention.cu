@@ -101,19 +101,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 }
 
 // Shared-memory plan (offsets in bytes from a 1024-aligned base).
-template <int D, int GQ>
+template <int D, int GQ, int W = kWarps>
 struct Plan {
   static constexpr int kTile = 64 * D;                    // one slot: 32 rows of D bf16
-  static constexpr int kRing = kWarps * kNST * kTile;
-  static constexpr int kBars = kRing;                      // kWarps * kNST mbarriers
-  static constexpr int kLists = kBars + 8 * kWarps * kNST; // kWarps * kListMax int32
-  static constexpr int kEnd = kLists + 4 * kWarps * kListMax;
+  static constexpr int kRing = W * kNST * kTile;
+  static constexpr int kBars = kRing;                      // W * kNST mbarriers
+  static constexpr int kLists = kBars + 8 * W * kNST;      // W * kListMax int32
+  static constexpr int kEnd = kLists + 4 * W * kListMax;
   // combine scratch (floats), aliased onto the ring once every stage is drained
   // (per-warp output rows padded to D + 4 floats: the fragment-order stores of
   // lanes with different t then fall in different banks)
   static constexpr int kOS = D + 4;
-  static constexpr int kWarpM = 0, kWarpL = kWarps * GQ, kWarpO = 2 * kWarps * GQ;
-  static constexpr int kCtaM = kWarpO + kWarps * GQ * kOS, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
+  static constexpr int kWarpM = 0, kWarpL = W * GQ, kWarpO = 2 * W * GQ;
+  static constexpr int kCtaM = kWarpO + W * GQ * kOS, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
   static constexpr int kScratchBytes = 4 * (kCtaO + GQ * D);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
@@ -197,16 +197,19 @@ __device__ __forceinline__ void attend_tile(uint32_t tile, int nv, const uint32_
 }
 
 // KS = D / 16 (k-steps of the QK product and m-tiles of the PV product);
-// NT = query tiles of 8 heads (GQ = 8 * NT columns).
-template <int KS, int NT>
-__global__ void __launch_bounds__(kThreads)
+// NT = query tiles of 8 heads (GQ = 8 * NT columns); W = warps per CTA (slot
+// partitions): 4, two CTAs per SM; 8, one CTA per SM with twice the copies in
+// flight, for layers with no more segments than SMs.
+template <int KS, int NT, int W>
+__global__ void __launch_bounds__(32 * W)
     k_attn(const __grid_constant__ CUtensorMap tmap, const uint16_t *__restrict__ q,
            const int32_t *__restrict__ table, int slots, const int32_t *__restrict__ seq_len, int Hkv, int G,
            float scale_log2, float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
   constexpr int D = 16 * KS;
   constexpr int GQ = 8 * NT;
   constexpr int kBoxes = D / 64;  // 64-dim boxes (128 bytes per row) per tile
-  using P = Plan<D, GQ>;
+  using P = Plan<D, GQ, W>;
+  constexpr int kW = W, kT = 32 * W;
   extern __shared__ unsigned char sm_raw[];
   const uint32_t raw_addr = smem_addr(sm_raw);
   unsigned char *sm = sm_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // this warp's non-empty slots, as (slot << 5 | valid tokens)
-  const int nw = CL * kWarps, gw = rank * kWarps + warp;
+  const int nw = CL * kW, gw = rank * kW + warp;
   const int nk = slots > gw ? (slots - gw + nw - 1) / nw : 0;
   const int32_t *trow = table + static_cast<int64_t>(s) * slots;
   int count = 0;
@@ -356,15 +359,15 @@ __global__ void __launch_bounds__(kThreads)
       }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += kThreads) {  // the padded columns qc >= G are never read
+  for (int idx = tid; idx < G * D; idx += kT) {  // the padded columns qc >= G are never read
     const int qc = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * GQ + qc]);
+    for (int w = 0; w < kW; ++w) M = fmaxf(M, wm[w * GQ + qc]);
     float acc = 0.0f, ls = 0.0f;
     if (M > -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < kW; ++w) {
         const float f = exp2f(wm[w * GQ + qc] - M);
         acc += f * wo[(w * GQ + qc) * P::kOS + d];
         ls += f * wl[w * GQ + qc];
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kThreads)
   {
     const int n_out = G * D, per = (n_out + CL - 1) / CL;
     const int e1 = min(n_out, (rank + 1) * per);
-    for (int idx = rank * per + tid; idx < e1; idx += kThreads) {
+    for (int idx = rank * per + tid; idx < e1; idx += kT) {
       const int qc = idx / D, d = idx % D;
       float mr[kMaxCluster], lr[kMaxCluster], orr[kMaxCluster];
 #pragma unroll
@@ -985,31 +988,29 @@ cudaError_t make_pool_map(CUtensorMap *tmap, const uint16_t *pool, int D, int S,
 // larger clusters lose more to co-scheduling than they gain, and deeper
 // per-warp rings or a persistent SM-balanced split with a separate merge kernel
 // were slower), enough that each list of `lists` per CTA fits.
-int cluster_size(int sms, int S, int slots, int lists) {
-  int CL = static_cast<int>(std::min<int64_t>(4, std::max<int64_t>(1, 2 * static_cast<int64_t>(sms) / S)));
+int cluster_size(int sms, int S, int slots, int lists, int ctas_per_sm = 2) {
+  int CL = static_cast<int>(
+      std::min<int64_t>(4, std::max<int64_t>(1, static_cast<int64_t>(ctas_per_sm) * sms / S)));
   CL = std::min(CL, slots);
   while ((slots + CL * lists - 1) / (CL * lists) > kListMax) ++CL;
   return CL;
 }
 
-template <int KS, int NT>
-cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
-                     const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
-                     int32_t *status, cudaStream_t st) {
+template <int KS, int NT, int W>
+cudaError_t launch_tw(const CUtensorMap &tmap, const uint16_t *q, const int32_t *table, int slots,
+                      const int32_t *seq_len, int S, int Hkv, int G, float scale, float *out, float *lse,
+                      int32_t *status, cudaStream_t st) {
   constexpr int D = 16 * KS;
-  using P = Plan<D, 8 * NT>;
-  const int S = B * Hkv;
-  CUtensorMap tmap;
-  cudaError_t me = make_pool_map(&tmap, pool, D, S, slots);
-  if (me != cudaSuccess) return me;
+  using P = Plan<D, 8 * NT, W>;
   const size_t smem = P::kEnd + 1024;  // + slack for the 1024-byte alignment of the swizzled tiles
   int sms = 0, per_sm = 0;
-  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<KS, NT>), kThreads, smem, &sms, &per_sm);
+  cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_attn<KS, NT, W>), 32 * W, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
-  // split each segment over a cluster of CL CTAs
-  const int CL = cluster_size(sms, S, slots, kWarps);
+  // split each segment over a cluster of CL CTAs (about 2 CTAs per SM in all at
+  // 4 warps, one at 8)
+  const int CL = cluster_size(sms, S, slots, W, W == 4 ? 2 : 1);
   if (CL > kMaxCluster) return cudaErrorInvalidValue;
-  LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(kThreads), smem, st);
+  LaunchCfg lc(dim3(static_cast<unsigned>(CL), static_cast<unsigned>(S)), dim3(32 * W), smem, st);
   cudaLaunchAttribute cl;
   cl.id = cudaLaunchAttributeClusterDimension;
   cl.val.clusterDim.x = static_cast<unsigned>(CL);
@@ -1017,8 +1018,32 @@ cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *tab
   cl.val.clusterDim.z = 1;
   lc.add(cl);
   const float scale_log2 = scale * 1.4426950408889634f;
-  return cudaLaunchKernelEx(&lc.cfg, k_attn<KS, NT>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out, lse,
-                            status);
+  return cudaLaunchKernelEx(&lc.cfg, k_attn<KS, NT, W>, tmap, q, table, slots, seq_len, Hkv, G, scale_log2, out,
+                            lse, status);
+}
+
+// Up to 8 query heads per KV head: 4-warp CTAs, about two per SM in all.  When
+// the segments fill more than half of the SMs but do not outnumber them, that
+// takes a cluster of two per segment; one CTA of 8 warps (one per SM, as many
+// copies in flight) instead needs no cluster merge (measured on GB300 at 128
+// segments: 26.8 -> 24.7 us).  With fewer segments the 8-warp CTAs would still
+// need clusters, and were slower (64 segments: 15.4 -> 15.5 us).
+template <int KS, int NT>
+cudaError_t launch_t(const uint16_t *q, const uint16_t *pool, const int32_t *table, int slots,
+                     const int32_t *seq_len, int B, int Hkv, int G, float scale, float *out, float *lse,
+                     int32_t *status, cudaStream_t st) {
+  constexpr int D = 16 * KS;
+  const int S = B * Hkv;
+  CUtensorMap tmap;
+  cudaError_t me = make_pool_map(&tmap, pool, D, S, slots);
+  if (me != cudaSuccess) return me;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (S <= sms && 2 * S > sms)
+    return launch_tw<KS, NT, 8>(tmap, q, table, slots, seq_len, S, Hkv, G, scale, out, lse, status, st);
+  return launch_tw<KS, NT, 4>(tmap, q, table, slots, seq_len, S, Hkv, G, scale, out, lse, status, st);
 }
 
 // More than 8 query heads per KV head: the head-split kernel (8 warps per CTA).

@@ -312,6 +312,43 @@ def test_stage_copies_exactly_the_plan():
 
 # ------------------------------------------------------------------ attention
 
+@pytest.mark.parametrize("D,G", [(128, 4), (64, 8), (128, 1)])
+def test_attention_one_cta_of_8_warps(D, G):
+    """Between half the SMs and all of them in segments (here 100 segments, or
+    the SM count if smaller), the attention runs one 8-warp CTA per segment;
+    ragged slot lists, empty slots and a partial last block as elsewhere."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Hkv = 4, max(1, min(sms, 100)) // 4
+    S = B * Hkv
+    rng = np.random.default_rng(700 + D + G)
+    Nb, slots = 64, 21
+    lens = np.array([16 * Nb - 3, 16 * 40 + 7, 16 * Nb, 5], dtype=np.int32)
+    tiles = _bf16_rand(rng, (S, Nb, 2, 16, D))
+    q = _bf16_rand(rng, (B, Hkv * G, D))
+    tables = np.full((S, slots), -1, np.int32)
+    for s in range(S):
+        blocks = rng.choice(Nb, size=slots, replace=False)
+        tables[s] = np.where(rng.random(slots) > 0.1, blocks, -1)
+    pool = np.zeros((S, slots, 2, 16, D), np.uint16)
+    for s in range(S):
+        for i, blk in enumerate(tables[s]):
+            if blk >= 0:
+                pool[s, i] = tiles[s, blk]
+    out = torch.full((B, Hkv * G, D), 9.0, dtype=torch.float32, device=DEV)
+    lse = torch.zeros((B, Hkv * G), dtype=torch.float32, device=DEV)
+    scale = default_scale(D)
+    st = _status()
+    okv.oasis_sparse_decode_attn(_dev_bf16(q), _dev_bf16(pool), torch.from_numpy(tables).to(DEV), slots,
+                                 torch.from_numpy(lens).to(DEV), B, Hkv, G, D, scale, out, lse, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    go, gl = out.cpu().numpy(), lse.cpu().numpy()
+    for s in range(S):
+        b, h = divmod(s, Hkv)
+        ro, rl = oattn.sparse_decode_attention(q[b, h * G:(h + 1) * G], pool[s], tables[s], int(lens[b]), scale)
+        assert_attention_close(go[b, h * G:(h + 1) * G], ro, gl[b, h * G:(h + 1) * G], rl)
+
+
 @pytest.mark.parametrize("mode", ["cluster", "ws", "tc"])
 # G > 8 runs the head-split kernel: (64, 12) its d_h 64 form, (128, 9) a second half
 # with one head, (128, 16, 3) slot partitions left empty.  The tcgen05 kernel (d_h
