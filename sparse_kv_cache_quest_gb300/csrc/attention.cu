@@ -114,7 +114,9 @@ struct Plan {
   static constexpr int kOS = D + 4;
   static constexpr int kWarpM = 0, kWarpL = W * GQ, kWarpO = 2 * W * GQ;
   static constexpr int kCtaM = kWarpO + W * GQ * kOS, kCtaL = kCtaM + GQ, kCtaO = kCtaL + GQ;
-  static constexpr int kScratchBytes = 4 * (kCtaO + GQ * D);
+  // per query column: each warp's merge factor 2^(m_w - M), then 1 / l
+  static constexpr int kHeadF = kCtaO + GQ * D, kHeadInv = kHeadF + GQ * W;
+  static constexpr int kScratchBytes = 4 * (kHeadInv + GQ);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
 
@@ -359,31 +361,36 @@ __global__ void __launch_bounds__(32 * W)
       }
   }
   __syncthreads();
-  for (int idx = tid; idx < G * D; idx += kT) {  // the padded columns qc >= G are never read
-    const int qc = idx / D, d = idx % D;
+  // per query column (once, not once per output): the warps' merge factors
+  // 2^(m_w - M), the CTA's M and l, and 1 / l
+  float *hf = scratch + P::kHeadF, *hinv = scratch + P::kHeadInv;
+  for (int qc = tid; qc < G; qc += kT) {  // the padded columns qc >= G are never read
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kW; ++w) M = fmaxf(M, wm[w * GQ + qc]);
-    float acc = 0.0f, ls = 0.0f;
-    if (M > -INFINITY) {
+    float ls = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kW; ++w) {
-        const float f = exp2f(wm[w * GQ + qc] - M);
-        acc += f * wo[(w * GQ + qc) * P::kOS + d];
-        ls += f * wl[w * GQ + qc];
-      }
+    for (int w = 0; w < kW; ++w) {
+      const float f = M > -INFINITY ? exp2f(wm[w * GQ + qc] - M) : 0.0f;
+      hf[qc * kW + w] = f;
+      ls += f * wl[w * GQ + qc];
     }
-    if (CL == 1) {  // one CTA: its totals are the results (the cluster merge would scale them by 2^0)
-      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
-      out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
-      if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
-      continue;
-    }
-    co[qc * D + d] = acc;
-    if (d == 0) {
-      cm[qc] = M;
-      cl[qc] = ls;
-    }
+    cm[qc] = M;
+    cl[qc] = ls;
+    hinv[qc] = ls > 0.0f ? 1.0f / ls : 0.0f;
+    if (CL == 1 && lse != nullptr)
+      lse[static_cast<int64_t>(bseq) * Hq + h * G + qc] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kT) {
+    const int qc = idx / D, d = idx % D;
+    float acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) acc += hf[qc * kW + w] * wo[(w * GQ + qc) * P::kOS + d];
+    if (CL == 1)  // one CTA: its totals are the results
+      out[(static_cast<int64_t>(bseq) * Hq + h * G + qc) * D + d] = hinv[qc] > 0.0f ? acc * hinv[qc] : 0.0f;
+    else
+      co[qc * D + d] = acc;
   }
   if (CL == 1) return;  // no other CTA reads this one's shared memory
   cluster.sync();
@@ -456,7 +463,8 @@ struct PlanHS {
   static constexpr int kOS = D + 4;  // padded per-warp output rows, as in Plan
   static constexpr int kWarpM = 0, kWarpL = kWarpsHS * 8, kWarpO = 2 * kWarpsHS * 8;
   static constexpr int kCtaM = kWarpO + kWarpsHS * 8 * kOS, kCtaL = kCtaM + 16, kCtaO = kCtaL + 16;
-  static constexpr int kScratchBytes = 4 * (kCtaO + 16 * D);
+  static constexpr int kHeadF = kCtaO + 16 * D, kHeadInv = kHeadF + 16 * kPairs;  // as in Plan
+  static constexpr int kScratchBytes = 4 * (kHeadInv + 16);
   static_assert(kScratchBytes <= kRing, "combine scratch must fit in the ring");
 };
 
@@ -629,32 +637,37 @@ __global__ void __launch_bounds__(kThreadsHS)
   __syncthreads();
   // head qc = 8 * half + j was processed by warps half * kPairs + p, p = 0..kPairs-1
   // (combined in that order, as k_attn combines its warps)
-  for (int idx = tid; idx < G * D; idx += kThreadsHS) {
-    const int qc = idx / D, d = idx % D;
+  // per query column first (as in k_attn), then the outputs
+  float *hf = scratch + P::kHeadF, *hinv = scratch + P::kHeadInv;
+  for (int qc = tid; qc < G; qc += kThreadsHS) {
     const int w0 = (qc >> 3) * kPairs, j = qc & 7;
     float M = -INFINITY;
 #pragma unroll
     for (int p = 0; p < kPairs; ++p) M = fmaxf(M, wm[(w0 + p) * 8 + j]);
-    float acc = 0.0f, ls = 0.0f;
-    if (M > -INFINITY) {
+    float ls = 0.0f;
 #pragma unroll
-      for (int p = 0; p < kPairs; ++p) {
-        const float f = exp2f(wm[(w0 + p) * 8 + j] - M);
-        acc += f * wo[((w0 + p) * 8 + j) * P::kOS + d];
-        ls += f * wl[(w0 + p) * 8 + j];
-      }
+    for (int p = 0; p < kPairs; ++p) {
+      const float f = M > -INFINITY ? exp2f(wm[(w0 + p) * 8 + j] - M) : 0.0f;
+      hf[qc * kPairs + p] = f;
+      ls += f * wl[(w0 + p) * 8 + j];
     }
-    if (CL == 1) {  // one CTA: its totals are the results (the cluster merge would scale them by 2^0)
-      const int64_t row = static_cast<int64_t>(bseq) * Hq + h * G + qc;
-      out[row * D + d] = ls > 0.0f ? acc / ls : 0.0f;
-      if (d == 0 && lse != nullptr) lse[row] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
-      continue;
-    }
-    co[qc * D + d] = acc;
-    if (d == 0) {
-      cm[qc] = M;
-      cl[qc] = ls;
-    }
+    cm[qc] = M;
+    cl[qc] = ls;
+    hinv[qc] = ls > 0.0f ? 1.0f / ls : 0.0f;
+    if (CL == 1 && lse != nullptr)
+      lse[static_cast<int64_t>(bseq) * Hq + h * G + qc] = ls > 0.0f ? (M + log2f(ls)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += kThreadsHS) {
+    const int qc = idx / D, d = idx % D;
+    const int w0 = (qc >> 3) * kPairs, j = qc & 7;
+    float acc = 0.0f;
+#pragma unroll
+    for (int p = 0; p < kPairs; ++p) acc += hf[qc * kPairs + p] * wo[((w0 + p) * 8 + j) * P::kOS + d];
+    if (CL == 1)  // one CTA: its totals are the results
+      out[(static_cast<int64_t>(bseq) * Hq + h * G + qc) * D + d] = hinv[qc] > 0.0f ? acc * hinv[qc] : 0.0f;
+    else
+      co[qc * D + d] = acc;
   }
   if (CL == 1) return;  // no other CTA reads this one's shared memory
   cluster.sync();
