@@ -30,19 +30,22 @@
 // all segments form one range, split evenly over a persistent grid of two CTAs
 // per SM (two MMA lanes and rings side by side: a lane blocks while its MMAs
 // run, and each CTA holds one query-operand buffer, rebuilt when its segment
-// changes).  A tile is moved in two halves (its kmax chunks, then its kmin
-// chunks; 32 KiB each at d_h 128) through a ring of half-tile stages.  Roles in
-// a CTA (warp-specialised, mbarrier hand-offs, every wait bounded):
-//   warp 0, one lane  - one 3-D TMA tensor copy per half-tile (a box of 16
-//                       chunks x 128 blocks x 8 dims of the chunk-major
+// changes).  A tile is moved as its kmax chunks, then its kmin chunks, each
+// half cut into kPieces pieces (16 KiB at d_h 128), through a ring of
+// piece-sized stages: a stage is held only while the few MMAs that read it run,
+// and the ring takes the shared memory left beside the query operand in smaller
+// units.  Roles in a CTA (warp-specialised, mbarrier hand-offs, every wait
+// bounded):
+//   warp 0, one lane  - one 3-D TMA tensor copy per piece (a box of CH /
+//                       kPieces chunks x 128 blocks x 8 dims of the chunk-major
 //                       summaries; 16-byte bulk copies per chunk when the block
 //                       count is not a multiple of 8);
-//   warp 1, one lane  - D/16 MMAs per half-tile into one of four TMEM
+//   warp 1, one lane  - the piece's MMAs (K = 16 each) into one of four TMEM
 //                       accumulators (the warp also owns the TMEM allocation);
 //   warps 2-5 (scan)  - per segment, the split query operand {q+, q-} in the
 //                       no-swizzle K-major layout, Q_d and max_d Q_d (built
 //                       once the previous segment's MMAs are done); without wrong-side
-//                       sums also, per half-tile, C_b's share from the stage
+//                       sums also, per piece, C_b's share from the stage
 //                       (each thread one block row), after which the stage is
 //                       released, and C_b to the TMEM warps through a small ring;
 //   warps 6-9 (TMEM)  - the accumulator row (tcgen05.ld), the max over the
@@ -54,7 +57,7 @@
 // the MMAs it issues).
 // Shared-memory operands use the no-swizzle K-major layout of 8-row x 16-byte
 // core matrices: the chunk-major summaries already are that layout (chunk c of
-// 128 blocks = 16 core matrices at 128-byte steps), so a half-tile lands as is:
+// 128 blocks = 16 core matrices at 128-byte steps), so a piece lands as is:
 // LBO (next 8 K-elements) = 2048 bytes, SBO (next 8 rows) = 128.
 #include <algorithm>
 #include <cfloat>
@@ -75,7 +78,8 @@ constexpr int kCtasPerSm = 2;                 // CTAs per SM: two MMA lanes and 
 constexpr int kMaxRegsTC = 80;                // registers a thread (see the kernel)
 constexpr int kBBufs = 1;                     // query-operand buffers per CTA
 constexpr size_t kSmemCap = (228 * 1024) / kCtasPerSm - 1024;  // per CTA (1 KiB of each SM's share is reserved)
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
+constexpr int kPieces = 2;                    // ring stages (pieces) per half-tile
 
 // ---- tcgen05 / TMEM primitives (inline PTX, sm_100a family) -----------------
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -214,13 +218,15 @@ __global__ void __maxnreg__(kMaxRegsTC)
                int G, int Nd, const int32_t *__restrict__ seq_len, int W, float *__restrict__ scores,
                float *__restrict__ radius, int32_t *status, int tps, int stages) {
   constexpr int D = CH * 8;
-  constexpr int KH = D / 16;                           // MMAs per half-tile (K = 16 each)
-  constexpr uint32_t kHalf = CH * kChunkBytes;         // one half-tile: the kmax chunks or the kmin chunks
+  constexpr int CP = CH / kPieces;                     // chunks per piece (a ring stage)
+  constexpr int KP = CP / 2;                           // MMAs per piece (K = 16 each)
+  constexpr uint32_t kPiece = CP * kChunkBytes;        // a piece: CP chunks of the kmax or the kmin half-tile
+  static_assert(CH % kPieces == 0 && CP % 2 == 0, "a piece holds whole MMA K-steps");
   constexpr uint32_t kBBytes = static_cast<uint32_t>(N) * 2 * D * 2;
   constexpr uint32_t kTmemCols = kNAcc * N <= 64 ? 64 : (kNAcc * N <= 128 ? 128 : 256);
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *sA = smem;                                               // [stages][kHalf]
-  uint8_t *sB = sA + static_cast<size_t>(stages) * kHalf;           // [kBBufs][kBBytes]
+  uint8_t *sA = smem;                                               // [stages][kPiece]
+  uint8_t *sB = sA + static_cast<size_t>(stages) * kPiece;          // [kBBufs][kBBytes]
   float *sQ = reinterpret_cast<float *>(sB + kBBufs * kBBytes);     // [2][D]
   float *sC = sQ + 2 * D;                                           // [kNC][kRows]
   float *sQmax = sC + kNC * kRows;                                  // [2]: max_d Q_d per query buffer
@@ -288,9 +294,9 @@ __global__ void __maxnreg__(kMaxRegsTC)
   }
 
   if (warp == 0) {
-    // ---------------- producer: one copy per half-tile into the stage ring
+    // ---------------- producer: one copy per piece into the stage ring
     if (lane == 0) {
-      int64_t issued = 0;    // half-tiles
+      int64_t issued = 0;    // pieces
       int st = 0;            // issued % stages
       uint32_t round = 0;    // issued / stages
       bool ok = true;
@@ -299,24 +305,25 @@ __global__ void __maxnreg__(kMaxRegsTC)
         const int base = it.j * kRows;
         const int rows = min(kRows, it.nc - base);
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
+        for (int q = 0; q < 2 * kPieces; ++q) {  // the kmax pieces, then the kmin pieces
+          const int h = q / kPieces, c0 = (q % kPieces) * CP;
           if (issued >= stages && !wait_or_abort(&empty[st], (round - 1u) & 1u, abort_flag)) {
             ok = false;
             break;
           }
-          uint8_t *dst = sA + static_cast<size_t>(st) * kHalf;
+          uint8_t *dst = sA + static_cast<size_t>(st) * kPiece;
           if (use_tma) {
-            // box {8 blocks x 8 dims, 16 groups of 8 blocks, CH chunks}: rows past
+            // box {8 blocks x 8 dims, 16 groups of 8 blocks, CP chunks}: rows past
             // the summary capacity arrive zero-filled, so the byte count is fixed
-            mbar_arrive_expect_tx(&full[st], kHalf);
-            tma_load_3d(dst, h == 0 ? &tmx : &tmn, 0, base / 8, s * CH, &full[st]);
+            mbar_arrive_expect_tx(&full[st], kPiece);
+            tma_load_3d(dst, h == 0 ? &tmx : &tmn, 0, base / 8, s * CH + c0, &full[st]);
           } else {
             const uint32_t bytes = static_cast<uint32_t>(rows) * 16u;
-            mbar_arrive_expect_tx(&full[st], CH * bytes);
+            mbar_arrive_expect_tx(&full[st], CP * bytes);
             const uint4 *g = reinterpret_cast<const uint4 *>(h == 0 ? kmax : kmin) +
-                             static_cast<int64_t>(s) * CH * Nb_max + base;
+                             static_cast<int64_t>(s * CH + c0) * Nb_max + base;
 #pragma unroll 4
-            for (int c = 0; c < CH; ++c)
+            for (int c = 0; c < CP; ++c)
               bulk_g2s(dst + c * kChunkBytes, g + static_cast<int64_t>(c) * Nb_max, bytes, &full[st]);
           }
           ++issued;
@@ -334,7 +341,7 @@ __global__ void __maxnreg__(kMaxRegsTC)
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16<N>();
-      int64_t i = 0, u = 0;  // tiles, half-tiles
+      int64_t i = 0, u = 0;  // tiles, pieces
       int st = 0;            // u % stages
       uint32_t round = 0;    // u / stages
       int seg_prev = -1, nseg = 0, buf = 0;
@@ -355,19 +362,19 @@ __global__ void __maxnreg__(kMaxRegsTC)
           break;
         const uint32_t b0 = smem_addr(sB + static_cast<size_t>(buf) * kBBytes);
 #pragma unroll 1
-        for (int h = 0; h < 2 && ok; ++h) {
+        for (int q = 0; q < 2 * kPieces && ok; ++q) {
           ok = wait_or_abort(&full[st], round & 1u, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a0 = smem_addr(sA + static_cast<size_t>(st) * kHalf);
+          const uint32_t a0 = smem_addr(sA + static_cast<size_t>(st) * kPiece);
 #pragma unroll
-          for (int kk = 0; kk < KH; ++kk) {
-            const int kg = h * KH + kk;  // K-step within the tile: kmax part, then kmin part
+          for (int kk = 0; kk < KP; ++kk) {
+            const int kg = q * KP + kk;  // K-step within the tile: kmax part, then kmin part
             const uint64_t da = smem_desc(a0 + kk * 2 * kChunkBytes, kChunkBytes, 128);
             const uint64_t db = smem_desc(b0 + kg * 2 * (N * 16), N * 16, 128);
             tc_mma(tmem + static_cast<uint32_t>(acc * N), da, db, idesc, kg > 0 ? 1u : 0u);
           }
-          tc_commit(&empty[st]);  // the half-stage is free once these MMAs have read it
+          tc_commit(&empty[st]);  // the stage is free once these MMAs have read it
           ++u;
           if (++st == stages) {
             st = 0;
@@ -474,8 +481,8 @@ __global__ void __maxnreg__(kMaxRegsTC)
       while (next_build <= s_last) build_next();
     } else {
       int64_t i = 0;         // tiles
-      int st = 0;            // half-tiles % stages
-      uint32_t round = 0;    // half-tiles / stages
+      int st = 0;            // pieces % stages
+      uint32_t round = 0;    // pieces / stages
       int seg_prev = -1, used = 0, bq = 0;
       for (it.begin(); it.valid(); it.advance()) {
         const int s = it.s;
@@ -492,15 +499,16 @@ __global__ void __maxnreg__(kMaxRegsTC)
         float C = 0.0f;
         {
 #pragma unroll 1
-          for (int h = 0; h < 2; ++h) {
+          for (int q = 0; q < 2 * kPieces; ++q) {
+            const int h = q / kPieces, c0 = (q % kPieces) * CP;
             const bool got = __all_sync(0xFFFFFFFFu, wait_or_abort(&full[st], round & 1u, abort_flag));
             if (got && row < rows) {
-              const uint8_t *A = sA + static_cast<size_t>(st) * kHalf + row * 16;
+              const uint8_t *A = sA + static_cast<size_t>(st) * kPiece + row * 16;
               // fast test: any sign bit set among the kmax half (h = 0) / any clear among
               // the kmin half (h = 1)?  (-0 and +0 pass it too; their magnitude is 0)
               uint32_t acc_or = 0u, acc_and = 0xFFFFFFFFu;
 #pragma unroll 8
-              for (int c = 0; c < CH; ++c) {
+              for (int c = 0; c < CP; ++c) {
                 const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
                 acc_or |= x.x | x.y | x.z | x.w;
                 acc_and &= x.x & x.y & x.z & x.w;
@@ -508,15 +516,16 @@ __global__ void __maxnreg__(kMaxRegsTC)
               const bool wrong = h == 0 ? (acc_or & 0x80008000u) != 0u : (acc_and & 0x80008000u) != 0x80008000u;
               if (wrong) {  // the exact weighted sum
                 const float *Q = sQ + bq * D;
-                for (int c = 0; c < CH; ++c) {
+                for (int c = 0; c < CP; ++c) {
                   const uint4 x = *reinterpret_cast<const uint4 *>(A + c * kChunkBytes);
                   const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                  const float *Qc = Q + (c0 + c) * 8;
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
                     const uint32_t m = neg_halves(xs[e]);
                     const uint32_t cw = h == 0 ? (xs[e] & m & 0x7FFF7FFFu) : (xs[e] & ~m);
-                    C = fmaf(Q[c * 8 + 2 * e], bf16_lo(cw), C);
-                    C = fmaf(Q[c * 8 + 2 * e + 1], bf16_hi(cw), C);
+                    C = fmaf(Qc[2 * e], bf16_lo(cw), C);
+                    C = fmaf(Qc[2 * e + 1], bf16_hi(cw), C);
                   }
                 }
               }
@@ -624,13 +633,13 @@ __global__ void __maxnreg__(kMaxRegsTC)
 
 // The summaries of one kind (kmin or kmax) as a 3-D tensor: x = 64 bf16 (8
 // consecutive blocks of one 8-dim chunk, 128 bytes), y = Nb_max / 8 groups of 8
-// blocks, z = S * CH chunks; one box = a half-tile.
+// blocks, z = S * CH chunks; one box = a piece (CH / kPieces chunks of 128 blocks).
 int make_summary_map(CUtensorMap *m, const uint16_t *base, int S, int CH, int Nb_max) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return -1;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(Nb_max / 8), static_cast<cuuint64_t>(S) * CH};
   const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(Nb_max) * 16};
-  const cuuint32_t box[3] = {64, kRows / 8, static_cast<cuuint32_t>(CH)};
+  const cuuint32_t box[3] = {64, kRows / 8, static_cast<cuuint32_t>(CH / kPieces)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -644,7 +653,7 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
                       const uint16_t *qdraft, int B, int Hkv, int G, int Nd, const int32_t *seq_len, int W,
                       float *scores, float *radius, int32_t *status, cudaStream_t st) {
   constexpr int D = CH * 8;
-  constexpr size_t kHalf = static_cast<size_t>(CH) * kChunkBytes;
+  constexpr size_t kPiece = static_cast<size_t>(CH / kPieces) * kChunkBytes;
   constexpr size_t kBBytes = static_cast<size_t>(N) * 2 * D * 2;
   const int S = B * Hkv;
   const int ncand = Nb_max - W;
@@ -657,9 +666,9 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
                        make_summary_map(&tmn, kmin, S, CH, Nb_max) == 0;
   const size_t fixed = kBBufs * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
                        (2 * kMaxStages + 2 * kNAcc + 8 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
-  const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kHalf));
+  const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kPiece));
   if (stages < 2) return cudaErrorInvalidValue;
-  const size_t smem = fixed + stages * kHalf;
+  const size_t smem = fixed + stages * kPiece;
   int sms = 0, per_sm = 0;
   cudaError_t e = launch_geometry(reinterpret_cast<const void *>(k_score_tc<N, CH>), kThreadsTC, smem, &sms, &per_sm);
   if (e != cudaSuccess) return e;
