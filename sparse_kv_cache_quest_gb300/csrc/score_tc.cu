@@ -30,14 +30,14 @@
 // all segments form one range, split evenly over a persistent grid of two CTAs
 // per SM (two MMA lanes and rings side by side: a lane blocks while its MMAs
 // run, and each CTA holds one query-operand buffer, rebuilt when its segment
-// changes).  A tile is moved as its kmax chunks, then its kmin chunks, each
-// half cut into kPieces pieces (16 KiB at d_h 128), through a ring of
-// piece-sized stages: a stage is held only while the few MMAs that read it run,
-// and the ring takes the shared memory left beside the query operand in smaller
-// units.  Roles in a CTA (warp-specialised, mbarrier hand-offs, every wait
-// bounded):
+// changes).  A tile is moved as its kmax chunks, then its kmin chunks, through
+// a ring of stages that each hold one piece of a half: the whole half, or,
+// where only two half-sized stages fit beside the query operand, half of it
+// (16 KiB at d_h 128), so that a stage is held only while the few MMAs that
+// read it run (pieces()).  Roles in a CTA (warp-specialised, mbarrier
+// hand-offs, every wait bounded):
 //   warp 0, one lane  - one 3-D TMA tensor copy per piece (a box of CH /
-//                       kPieces chunks x 128 blocks x 8 dims of the chunk-major
+//                       pieces chunks x 128 blocks x 8 dims of the chunk-major
 //                       summaries; 16-byte bulk copies per chunk when the block
 //                       count is not a multiple of 8);
 //   warp 1, one lane  - the piece's MMAs (K = 16 each) into one of four TMEM
@@ -79,7 +79,25 @@ constexpr int kMaxRegsTC = 80;                // registers a thread (see the ker
 constexpr int kBBufs = 1;                     // query-operand buffers per CTA
 constexpr size_t kSmemCap = (228 * 1024) / kCtasPerSm - 1024;  // per CTA (1 KiB of each SM's share is reserved)
 constexpr int kMaxStages = 16;
-constexpr int kPieces = 2;                    // ring stages (pieces) per half-tile
+
+// Shared memory of a CTA besides its ring: the query operand, Q (two slots),
+// the C_b ring, max_d Q_d (two slots), the barriers and the TMEM address.
+template <int N, int CH>
+constexpr size_t fixed_smem() {
+  return kBBufs * static_cast<size_t>(N) * 2 * (CH * 8) * 2 + (2 * CH * 8 + kNC * kRows + 2) * sizeof(float) +
+         (2 * kMaxStages + 2 * kNAcc + 8 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
+}
+// Ring stages (pieces) per half-tile.  Where only two half-tile stages fit
+// beside the query operand (32 to 64 query columns at d_h 128), a stage spends
+// a large share of its turn held under its MMAs; halves cut in two keep more of
+// the same ring in flight (235B-shaped layer, 64 columns: 47.8 -> 47.4 us).  With
+// three or more half-tile stages the extra copies and barrier rounds cost more
+// than that gains (Qwen3-8B-shaped step, 16 columns: 45.3-45.9 -> 47.1 us), so
+// the halves stay whole.
+template <int N, int CH>
+constexpr int pieces() {
+  return (kSmemCap - fixed_smem<N, CH>()) / (static_cast<size_t>(CH) * kChunkBytes) >= 3 ? 1 : 2;
+}
 
 // ---- tcgen05 / TMEM primitives (inline PTX, sm_100a family) -----------------
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -218,6 +236,7 @@ __global__ void __maxnreg__(kMaxRegsTC)
                int G, int Nd, const int32_t *__restrict__ seq_len, int W, float *__restrict__ scores,
                float *__restrict__ radius, int32_t *status, int tps, int stages) {
   constexpr int D = CH * 8;
+  constexpr int kPieces = pieces<N, CH>();
   constexpr int CP = CH / kPieces;                     // chunks per piece (a ring stage)
   constexpr int KP = CP / 2;                           // MMAs per piece (K = 16 each)
   constexpr uint32_t kPiece = CP * kChunkBytes;        // a piece: CP chunks of the kmax or the kmin half-tile
@@ -633,13 +652,13 @@ __global__ void __maxnreg__(kMaxRegsTC)
 
 // The summaries of one kind (kmin or kmax) as a 3-D tensor: x = 64 bf16 (8
 // consecutive blocks of one 8-dim chunk, 128 bytes), y = Nb_max / 8 groups of 8
-// blocks, z = S * CH chunks; one box = a piece (CH / kPieces chunks of 128 blocks).
-int make_summary_map(CUtensorMap *m, const uint16_t *base, int S, int CH, int Nb_max) {
+// blocks, z = S * CH chunks; one box = a piece (cp chunks of 128 blocks).
+int make_summary_map(CUtensorMap *m, const uint16_t *base, int S, int CH, int cp, int Nb_max) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return -1;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(Nb_max / 8), static_cast<cuuint64_t>(S) * CH};
   const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(Nb_max) * 16};
-  const cuuint32_t box[3] = {64, kRows / 8, static_cast<cuuint32_t>(CH / kPieces)};
+  const cuuint32_t box[3] = {64, kRows / 8, static_cast<cuuint32_t>(cp)};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -652,9 +671,8 @@ template <int N, int CH>
 cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *wsum, int Nb_max,
                       const uint16_t *qdraft, int B, int Hkv, int G, int Nd, const int32_t *seq_len, int W,
                       float *scores, float *radius, int32_t *status, cudaStream_t st) {
-  constexpr int D = CH * 8;
-  constexpr size_t kPiece = static_cast<size_t>(CH / kPieces) * kChunkBytes;
-  constexpr size_t kBBytes = static_cast<size_t>(N) * 2 * D * 2;
+  constexpr int kCP = CH / pieces<N, CH>();  // chunks per piece
+  constexpr size_t kPiece = static_cast<size_t>(kCP) * kChunkBytes;
   const int S = B * Hkv;
   const int ncand = Nb_max - W;
   if (ncand <= 0) return cudaSuccess;  // no candidate can exist
@@ -662,10 +680,9 @@ cudaError_t launch_tc(const uint16_t *kmin, const uint16_t *kmax, const float *w
   // A tile's rows read by the tensor copies may run past Nb_max (zero-filled);
   // the tensor view needs whole groups of 8 blocks, else 16-byte bulk copies
   CUtensorMap tmx{}, tmn{};
-  const bool use_tma = Nb_max % 8 == 0 && make_summary_map(&tmx, kmax, S, CH, Nb_max) == 0 &&
-                       make_summary_map(&tmn, kmin, S, CH, Nb_max) == 0;
-  const size_t fixed = kBBufs * kBBytes + (2 * D + kNC * kRows + 2) * sizeof(float) +
-                       (2 * kMaxStages + 2 * kNAcc + 8 + 2 * kNC + 1) * sizeof(uint64_t) + 16;
+  const bool use_tma = Nb_max % 8 == 0 && make_summary_map(&tmx, kmax, S, CH, kCP, Nb_max) == 0 &&
+                       make_summary_map(&tmn, kmin, S, CH, kCP, Nb_max) == 0;
+  const size_t fixed = fixed_smem<N, CH>();
   const int stages = static_cast<int>(std::min<size_t>(kMaxStages, (kSmemCap - fixed) / kPiece));
   if (stages < 2) return cudaErrorInvalidValue;
   const size_t smem = fixed + stages * kPiece;
