@@ -111,6 +111,32 @@ def test_wrong_side_sums_bound(name):
     assert np.all(got[:, nc:] == -7.0)
 
 
+# Summary capacities that are not a multiple of 8 blocks (as also in the
+# adversarial cases below, 700 blocks): the kernel then moves the summaries with
+# 16-byte bulk copies per chunk instead of tensor copies, in whole-half stages
+# (16 query columns, d_h 64) or in half-half pieces (32 and 64 columns at d_h
+# 128); lengths end inside a block and inside a tile.
+ODD = {
+    "odd-nb-16q-ragged": wl.WORKLOADS[2].with_(B=3, L=16 * 203),
+    "odd-nb-32q": wl.WORKLOADS[5].with_(B=1, Nd=2, L=16 * 301 - 5),
+    "odd-nb-64q": wl.WORKLOADS[5].with_(B=1, L=16 * 389 + 7),
+    "odd-nb-d64-64q": wl.WORKLOADS[5].with_(B=1, D=64, L=16 * 133),
+}
+
+
+@pytest.mark.parametrize("name", list(ODD))
+@pytest.mark.parametrize("with_wsum", [True, False])
+def test_estimates_within_radius_odd_capacity(name, with_wsum):
+    okv.load()
+    w = ODD[name]
+    assert w.Nb % 8 != 0
+    sl = wl.ragged_seq_lens(w, 16 * 129 + 3) if name.endswith("ragged") else None
+    _, sld, kmin, kmax, wsum = _summaries(w, sl)
+    qd = wl.drafts(w, 0).cuda()
+    exact, est, rad = _score_both(w, kmin, kmax, qd, sld, wsum if with_wsum else None)
+    _check_radius(w, sld, exact, est, rad)
+
+
 def test_estimates_within_radius_ragged_and_empty():
     okv.load()
     w = wl.WORKLOADS[2].with_(B=6)
