@@ -46,11 +46,6 @@ def device_tiles(w, layer, device="cuda", chunk=8):
     return out
 
 
-def oracle_summary(w, tiles_np, L):
-    kmin, kmax, ids = block_summary(tiles_np[:, 0], L)
-    return kmin, kmax, ids
-
-
 def oracle_topk_true(w, layer, s, tiles_np, L):
     """Top-K candidate list of segment s under the true query (oracle arithmetic)."""
     kmin, kmax, _ = block_summary(tiles_np[:, 0], L)
